@@ -1,0 +1,249 @@
+"""CPU oracle for the fine-grained FP8 GEMM path (TEST INFRASTRUCTURE ONLY).
+
+The arithmetic lives in ``fgf8_oracle.c`` (plain C, fp64 accumulation).  This
+module builds it with gcc and wraps it for numpy arrays.  It shares no code with
+the CUDA library and never imports it.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline`` leg may use it.
+
+Parity unpinned: none.  Every function is pinned by a ``-m "not gpu"`` test in
+``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+SCALE_F32 = 0
+SCALE_UE8M0 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fgf8_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libfgf8_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when available). Returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+            "-fno-fast-math", _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        L = ctypes.c_long
+        I = ctypes.c_int
+        lib.fgo_e4m3_decode.restype = ctypes.c_double
+        lib.fgo_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.fgo_e4m3_encode.restype = ctypes.c_uint8
+        lib.fgo_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.fgo_e4m3_encode_array.argtypes = [P, P, L]
+        lib.fgo_e4m3_decode_array.argtypes = [P, P, L]
+        lib.fgo_align4.restype = L
+        lib.fgo_align4.argtypes = [L]
+        lib.fgo_quantize_1x128.argtypes = [P, L, L, I, P, P]
+        lib.fgo_quantize_128x128.argtypes = [P, L, L, L, I, P, P]
+        lib.fgo_gemm_fp8.argtypes = [P, P, P, P, L, L, L, I, P]
+        lib.fgo_gemm_fp8_entries.argtypes = [P, P, P, P, L, L, L, I, P, P, L, P]
+        lib.fgo_grouped_contiguous.argtypes = [P, P, P, P, P, L, L, L, L, I, P, P]
+        lib.fgo_grouped_masked.argtypes = [P, P, P, P, P, L, L, L, L, I, P, P]
+        lib.fgo_gemm_f16.argtypes = [P, P, L, L, L, P]
+        lib.fgo_gemm_f16_entries.argtypes = [P, P, L, L, L, P, P, L, P]
+        lib.fgo_num_threads.restype = I
+        lib.fgo_set_num_threads.argtypes = [I]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _f32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _u8(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+
+
+def _sf_buffer(sf) -> np.ndarray:
+    """Scale tables travel as raw bytes (float32 or packed int32)."""
+    a = np.ascontiguousarray(np.asarray(sf))
+    return a
+
+
+def align4(x: int) -> int:
+    return (int(x) + 3) // 4 * 4
+
+
+def num_threads() -> int:
+    return int(_load().fgo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().fgo_set_num_threads(int(n))
+
+
+# --------------------------------------------------------------------------- E4M3
+def e4m3_decode(codes) -> np.ndarray:
+    q = _u8(codes)
+    out = np.empty(q.shape, dtype=np.float64)
+    _load().fgo_e4m3_decode_array(_ptr(q), _ptr(out), q.size)
+    return out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64))
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().fgo_e4m3_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+# --------------------------------------------------------------------------- scales
+def sfa_shape(M: int, K: int, fmt: int):
+    """(rows, cols, dtype) of an activation scale table for M rows."""
+    nkb = K // 128
+    if fmt == SCALE_F32:
+        return (nkb, align4(M)), np.float32
+    return ((nkb + 3) // 4, align4(M)), np.int32
+
+
+def sfb_shape(G: int, N: int, K: int, fmt: int):
+    nkb = K // 128
+    if fmt == SCALE_F32:
+        return (G, (N + 127) // 128, nkb), np.float32
+    return (G, (nkb + 3) // 4, align4(N)), np.int32
+
+
+def quantize_1x128(X, fmt: int):
+    """X: (M, K) float32 (bf16 values). Returns (Xq uint8 (M,K), SFA)."""
+    x = _f32(X)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), dtype=np.uint8)
+    shape, dt = sfa_shape(M, K, fmt)
+    sf = np.empty(shape, dtype=dt)
+    _load().fgo_quantize_1x128(_ptr(x), M, K, fmt, _ptr(q), _ptr(sf))
+    return q, sf
+
+
+def quantize_128x128(W, fmt: int):
+    """W: (G, N, K) or (N, K) float32. Returns (Wq, SFB) with a leading G axis."""
+    w = _f32(W)
+    if w.ndim == 2:
+        w = w[None]
+    G, N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((G, N, K), dtype=np.uint8)
+    shape, dt = sfb_shape(G, N, K, fmt)
+    sf = np.empty(shape, dtype=dt)
+    _load().fgo_quantize_128x128(_ptr(w), G, N, K, fmt, _ptr(q), _ptr(sf))
+    return q, sf
+
+
+# --------------------------------------------------------------------------- GEMM
+def gemm_fp8(Aq, SFA, Bq, SFB, fmt: int) -> np.ndarray:
+    a = _u8(Aq)
+    b = _u8(Bq)
+    if b.ndim == 3:
+        assert b.shape[0] == 1
+        b = b[0]
+    M, K = a.shape
+    N = b.shape[0]
+    sfa = _sf_buffer(SFA)
+    sfb = _sf_buffer(SFB)
+    D = np.empty((M, N), dtype=np.float64)
+    _load().fgo_gemm_fp8(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), M, N, K, fmt, _ptr(D))
+    return D
+
+
+def gemm_fp8_entries(Aq, SFA, Bq, SFB, fmt: int, rows, cols) -> np.ndarray:
+    a = _u8(Aq)
+    b = _u8(Bq)
+    if b.ndim == 3:
+        assert b.shape[0] == 1
+        b = b[0]
+    M, K = a.shape
+    N = b.shape[0]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    assert r.shape == c.shape
+    out = np.empty(r.shape, dtype=np.float64)
+    _load().fgo_gemm_fp8_entries(_ptr(a), _ptr(_sf_buffer(SFA)), _ptr(b), _ptr(_sf_buffer(SFB)),
+                                 M, N, K, fmt, _ptr(r), _ptr(c), r.size, _ptr(out))
+    return out
+
+
+def grouped_contiguous(Aq, SFA, Bq, SFB, m_indices, fmt: int):
+    """Returns (D float64 (M,N), valid uint8 (M,N))."""
+    a = _u8(Aq)
+    b = _u8(Bq)
+    G, N, K = b.shape
+    M = a.shape[0]
+    mi = np.ascontiguousarray(np.asarray(m_indices, dtype=np.int32))
+    assert mi.shape == (M,)
+    D = np.zeros((M, N), dtype=np.float64)
+    valid = np.zeros((M, N), dtype=np.uint8)
+    _load().fgo_grouped_contiguous(_ptr(a), _ptr(_sf_buffer(SFA)), _ptr(b), _ptr(_sf_buffer(SFB)),
+                                   _ptr(mi), M, N, K, G, fmt, _ptr(D), _ptr(valid))
+    return D, valid
+
+
+def grouped_masked(Aq, SFA, Bq, SFB, masked_m, fmt: int):
+    """Aq: (G, Mmax, K). Returns (D float64 (G,Mmax,N), valid uint8)."""
+    a = _u8(Aq)
+    b = _u8(Bq)
+    G, Mmax, K = a.shape
+    N = b.shape[1]
+    mm = np.ascontiguousarray(np.asarray(masked_m, dtype=np.int32))
+    assert mm.shape == (G,)
+    D = np.zeros((G, Mmax, N), dtype=np.float64)
+    valid = np.zeros((G, Mmax, N), dtype=np.uint8)
+    _load().fgo_grouped_masked(_ptr(a), _ptr(_sf_buffer(SFA)), _ptr(b), _ptr(_sf_buffer(SFB)),
+                               _ptr(mm), G, Mmax, N, K, fmt, _ptr(D), _ptr(valid))
+    return D, valid
+
+
+def gemm_f16(A, B) -> np.ndarray:
+    a = _f32(A)
+    b = _f32(B)
+    M, K = a.shape
+    N = b.shape[0]
+    D = np.empty((M, N), dtype=np.float64)
+    _load().fgo_gemm_f16(_ptr(a), _ptr(b), M, N, K, _ptr(D))
+    return D
+
+
+def gemm_f16_entries(A, B, rows, cols) -> np.ndarray:
+    a = _f32(A)
+    b = _f32(B)
+    M, K = a.shape
+    N = b.shape[0]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    out = np.empty(r.shape, dtype=np.float64)
+    _load().fgo_gemm_f16_entries(_ptr(a), _ptr(b), M, N, K, _ptr(r), _ptr(c), r.size, _ptr(out))
+    return out
