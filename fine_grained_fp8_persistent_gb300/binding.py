@@ -1,0 +1,237 @@
+"""ctypes binding of libfgf8.so (include/fgf8.h).
+
+Argument marshalling only: shapes and raw device pointers go to the C ABI, the
+caller's current torch CUDA stream is passed as the stream, and outputs are
+allocated with torch.empty when the caller does not provide them.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.  If
+the library has not been built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfgf8.so")
+
+SCALE_F32 = 0
+SCALE_UE8M0 = 1
+F16 = 0
+BF16 = 1
+
+OK = 0
+ERR_DEVICE_TIMEOUT = 5
+ERR_DEVICE_INPUT = 6
+
+
+class FGF8Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (fgf8 status {code})")
+        self.code = code
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_LL = ctypes.c_longlong
+
+_SIGS = {
+    "quantize_1x128": ([_P, _P, _P, _I, _I, _I, _P], _I),
+    "quantize_128x128": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gemm_f16": ([_P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "gemm_fp8_blockscaled": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "grouped_fp8_contiguous": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "grouped_fp8_masked": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "fgf8_mk_alignment_for_contiguous": ([], _I),
+    "fgf8_sfa_bytes": ([_I, _I, _I], _LL),
+    "fgf8_sfb_bytes": ([_I, _I, _I, _I], _LL),
+    "fgf8_check_status": ([_P, ctypes.POINTER(ctypes.c_uint)], _I),
+    "fgf8_last_error": ([], ctypes.c_char_p),
+    "fgf8_set_wait_timeout_ms": ([_I], _I),
+    "fgf8_version": ([], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (for callers that pass raw pointers)."""
+    return _lib
+
+
+def last_error() -> str:
+    return (_lib.fgf8_last_error() or b"").decode()
+
+
+def _check(rc: int, name: str) -> None:
+    if rc != OK:
+        raise FGF8Error(rc, f"{name}: {last_error()}")
+
+
+def _fmt(fmt) -> int:
+    if isinstance(fmt, str):
+        return {"f32": SCALE_F32, "fp32": SCALE_F32, "ue8m0": SCALE_UE8M0}[fmt.lower()]
+    return int(fmt)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _u8(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+def align4(x: int) -> int:
+    return (int(x) + 3) // 4 * 4
+
+
+def sfa_shape(rows: int, K: int, fmt) -> tuple[tuple[int, ...], torch.dtype]:
+    nkb = K // 128
+    if _fmt(fmt) == SCALE_F32:
+        return (nkb, align4(rows)), torch.float32
+    return ((nkb + 3) // 4, align4(rows)), torch.int32
+
+
+def sfb_shape(G: int, N: int, K: int, fmt) -> tuple[tuple[int, ...], torch.dtype]:
+    nkb = K // 128
+    if _fmt(fmt) == SCALE_F32:
+        return (G, (N + 127) // 128, nkb), torch.float32
+    return (G, (nkb + 3) // 4, align4(N)), torch.int32
+
+
+# --------------------------------------------------------------------------- quantize
+def quantize_1x128(x: torch.Tensor, fmt, xq: torch.Tensor | None = None,
+                   sfa: torch.Tensor | None = None, stream=None):
+    """bf16 (M, K) -> (E4M3 codes uint8 (M, K), activation scale table)."""
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sfa is None:
+        shape, dt = sfa_shape(M, K, fmt)
+        sfa = torch.empty(shape, dtype=dt, device=x.device)
+    _check(_lib.quantize_1x128(_ptr(x), _ptr(_u8(xq)), _ptr(sfa), M, K, _fmt(fmt), _stream(stream)),
+           "quantize_1x128")
+    return xq, sfa
+
+
+def quantize_128x128(w: torch.Tensor, fmt, wq: torch.Tensor | None = None,
+                     sfb: torch.Tensor | None = None, stream=None):
+    """bf16 (N, K) or (G, N, K) -> (E4M3 codes, weight scale table with a G axis)."""
+    G, N, K = (1, *w.shape) if w.dim() == 2 else w.shape
+    if wq is None:
+        wq = torch.empty(tuple(w.shape), dtype=torch.uint8, device=w.device)
+    if sfb is None:
+        shape, dt = sfb_shape(G, N, K, fmt)
+        sfb = torch.empty(shape, dtype=dt, device=w.device)
+    _check(_lib.quantize_128x128(_ptr(w), _ptr(_u8(wq)), _ptr(sfb), G, N, K, _fmt(fmt),
+                                 _stream(stream)), "quantize_128x128")
+    return wq, sfb
+
+
+# --------------------------------------------------------------------------- GEMM
+def gemm_f16(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype | None = None,
+             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = A B^T for fp16/bf16 A (M, K), B (N, K); FP32 accumulation."""
+    M, K = a.shape
+    N = b.shape[0]
+    if a.dtype != b.dtype or a.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("A and B must both be fp16 or both bf16")
+    out_dtype = out_dtype or a.dtype
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    in_code = BF16 if a.dtype == torch.bfloat16 else F16
+    out_code = BF16 if out.dtype == torch.bfloat16 else F16
+    _check(_lib.gemm_f16(_ptr(a), _ptr(b), _ptr(out), M, N, K, in_code, out_code, _stream(stream)),
+           "gemm_f16")
+    return out
+
+
+def gemm_fp8_blockscaled(aq, sfa, bq, sfb, fmt, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """D (bf16, M x N) from E4M3 A (M, K) / B (N, K) with fine-grained scales."""
+    M, K = aq.shape
+    N = bq.shape[-2]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    _check(_lib.gemm_fp8_blockscaled(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(out),
+                                     M, N, K, _fmt(fmt), _stream(stream)), "gemm_fp8_blockscaled")
+    return out
+
+
+def grouped_fp8_contiguous(aq, sfa, bq, sfb, m_indices, fmt, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Contiguous-layout MoE GEMM: rows of expert g use B[g]; m_indices -1 = padding."""
+    M, K = aq.shape
+    G, N, _ = bq.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    if m_indices.dtype != torch.int32:
+        raise ValueError("m_indices must be int32")
+    _check(_lib.grouped_fp8_contiguous(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
+                                       _ptr(m_indices), _ptr(out), M, N, K, G, _fmt(fmt),
+                                       _stream(stream)), "grouped_fp8_contiguous")
+    return out
+
+
+def grouped_fp8_masked(aq, sfa, bq, sfb, masked_m, fmt, expected_m: int = 0,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Masked-layout MoE GEMM: A (G, Mmax, K); rows >= masked_m[g] are not computed."""
+    G, Mmax, K = aq.shape
+    N = bq.shape[1]
+    if out is None:
+        out = torch.empty((G, Mmax, N), dtype=torch.bfloat16, device=aq.device)
+    if masked_m.dtype != torch.int32:
+        raise ValueError("masked_m must be int32")
+    _check(_lib.grouped_fp8_masked(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
+                                   _ptr(masked_m), _ptr(out), G, Mmax, N, K, int(expected_m),
+                                   _fmt(fmt), _stream(stream)), "grouped_fp8_masked")
+    return out
+
+
+# --------------------------------------------------------------------------- utilities
+def check_status(stream=None) -> tuple[int, int]:
+    """Synchronise the stream; return (status code, raw device status bits)."""
+    bits = ctypes.c_uint(0)
+    rc = _lib.fgf8_check_status(_stream(stream), ctypes.byref(bits))
+    return rc, bits.value
+
+
+def mk_alignment_for_contiguous() -> int:
+    return int(_lib.fgf8_mk_alignment_for_contiguous())
+
+
+def sfa_bytes(rows: int, K: int, fmt) -> int:
+    return int(_lib.fgf8_sfa_bytes(rows, K, _fmt(fmt)))
+
+
+def sfb_bytes(G: int, N: int, K: int, fmt) -> int:
+    return int(_lib.fgf8_sfb_bytes(G, N, K, _fmt(fmt)))
+
+
+def set_wait_timeout_ms(ms: int) -> int:
+    return int(_lib.fgf8_set_wait_timeout_ms(int(ms)))
+
+
+def version() -> int:
+    return int(_lib.fgf8_version())

@@ -1,0 +1,65 @@
+// fgf8_internal.h -- declarations shared by the library's translation units (not
+// part of the public ABI; the public header is include/fgf8.h).
+#pragma once
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+// Bits of the per-device status word written by kernels.
+#define FGF8_DEVERR_TIMEOUT 0x1u      // a bounded barrier wait ran out
+#define FGF8_DEVERR_INPUT 0x2u        // device-side input out of contract (m_indices / masked_m)
+#define FGF8_DEVERR_ROLE_PRODUCER 0x100u
+#define FGF8_DEVERR_ROLE_MMA 0x200u
+#define FGF8_DEVERR_ROLE_EPILOGUE 0x400u
+
+#ifndef __CUDACC_RTC__
+namespace fgf8 {
+
+enum class Kind : int { F16 = 0, MXF8 = 1, F8F32 = 2 };
+enum class Sched : int { Dense = 0, Contiguous = 1, Masked = 2 };
+
+// Everything a GEMM launch needs besides the tensor maps.
+struct GemmArgs {
+  int M;              // rows of A (dense/contiguous) or Mmax (masked)
+  int N;              // columns of D (per expert)
+  int K;              // reduction length
+  int G;              // experts (1 for dense)
+  const int32_t* m_indices;   // contiguous: expert of each row, -1 = padding
+  const int32_t* masked_m;    // masked: valid rows per expert (device memory)
+  void* D;                    // output, row-major, leading dimension N
+  int in_bf16;                // 16-bit GEMM operands: 1 bf16, 0 fp16
+  int out_bf16;               // 1: bf16 output, 0: fp16 output
+  const float* sfa_f32;       // FP32-scale path: activation scales
+  const float* sfb_f32;       // FP32-scale path: weight block scales
+  uint32_t* status;           // device status word
+  uint64_t timeout_ns;        // bound on every barrier wait
+};
+
+struct TensorMaps {
+  CUtensorMap a, b, sfa, sfb;
+};
+
+// Host helpers (host.cu).
+int set_error(int code, const char* fmt, ...);
+int device_sm_count();
+int device_max_smem_optin();
+uint32_t* device_status_ptr();
+uint64_t wait_timeout_ns();
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                    uint32_t box_outer, bool swizzle128);
+
+// Launchers (one translation unit each).
+int launch_gemm_f16(const GemmArgs& a, const void* A, const void* B, cudaStream_t stream);
+int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
+                     const void* Bq, const void* SFB, cudaStream_t stream);
+int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
+                      cudaStream_t stream);
+int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int fmt,
+                          cudaStream_t stream);
+int launch_quantize_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, int fmt,
+                            cudaStream_t stream);
+
+}  // namespace fgf8
+#endif

@@ -1,0 +1,191 @@
+/*
+ * fgf8.h -- C ABI of the fine-grained FP8 persistent GEMM library for GB300
+ * (sm_103a).  Library file: libfgf8.so.
+ *
+ * What it computes: the NT GEMM D = A * B^T (the linear layer Y = X W^T) with
+ * FP32 accumulation, for 16-bit operands and for E4M3 operands carrying
+ * DeepSeek-V3 fine-grained scales (1x128 per token for A, 128x128 per block for
+ * B), plus the contiguous and masked grouped MoE forms and the quantizers that
+ * produce the E4M3 operands.  Page references name the web page and section:
+ *   [DG]   "DeepGEMM dissected: a 300-line FP8 GEMM kernel" (pinghaoyang.com.cn)
+ *   [TC5]  "GPU GEMM part 4: tcgen05 & Blackwell" (pinghaoyang.com.cn)
+ *   [TIRx] "TIRx and high-performance GEMM (part 2)" (Tencent Cloud developer)
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps them.  Each must be 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and returns as soon as the work is
+ *     enqueued.
+ *   - Arguments are validated on the host first.  An invalid call returns a
+ *     non-zero fgf8_status and launches nothing; fgf8_last_error() then gives a
+ *     message.  Validation needs no GPU.
+ *   - Device-side problems (a device-side input out of contract, or a bounded
+ *     pipeline wait that ran out) set bits in a per-device status word read by
+ *     fgf8_check_status().  After such an error the output is undefined.
+ *   - Row-major layouts; "NT": A is (M, K) with K contiguous, B is (N, K) with K
+ *     contiguous ([DG] "why only the NT layout").
+ *   - Empty problems (M == 0, or every masked row count 0) are valid no-ops.
+ *
+ * Scale-table layouts (fmt = FGF8_SCALE_F32 or FGF8_SCALE_UE8M0), with
+ * nkb = K / 128 (K must be a multiple of 128, [DG] "thread organisation":
+ * BLOCK_K is fixed at 128, the scale granularity):
+ *   activation scales SFA for R rows (the 1x128 groups of [DG] "fine-grained
+ *   quantization", stored TMA-aligned and transposed, [DG] "why only the NT
+ *   layout"):
+ *     F32   : float  [nkb][align4(R)]   entry (kb, r) = scale of row r, K block kb
+ *     UE8M0 : int32  [ceil(nkb/4)][align4(R)]; byte (kb % 4) of word (kb / 4, r)
+ *             is the biased exponent e + 127 of the power-of-two scale 2^e;
+ *             bytes of K blocks >= nkb and rows >= R are 0.
+ *   weight scales SFB for G experts of N rows (128x128 blocks):
+ *     F32   : float  [G][ceil(N/128)][nkb]   one scale per 128x128 block
+ *     UE8M0 : int32  [G][ceil(nkb/4)][align4(N)]; the block exponent is stored
+ *             for every row n of its block (the MMA reads one scale per B row,
+ *             [TC5] section 6 block-scaling formula with SFB(N, SFK)).
+ *   align4(x) = ceil(x / 4) * 4.
+ * F32 scales are s = amax / 448 (FP32); UE8M0 scales are 2^e with
+ * e = ceil(log2(amax / 448)) clamped to [-127, 127]; an all-zero group has
+ * scale 1.  E4M3 codes are round-to-nearest-even, saturating at +-448.
+ */
+#ifndef FGF8_H
+#define FGF8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FGF8_API __attribute__((visibility("default")))
+#else
+#define FGF8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FGF8_OK = 0,
+  FGF8_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size */
+  FGF8_ERR_UNSUPPORTED = 2,   /* shape or option outside what the kernels support */
+  FGF8_ERR_MISALIGNED = 3,    /* pointer or leading dimension not 16-byte aligned */
+  FGF8_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  FGF8_ERR_DEVICE_TIMEOUT = 5,/* fgf8_check_status: a kernel's bounded wait ran out */
+  FGF8_ERR_DEVICE_INPUT = 6   /* fgf8_check_status: m_indices / masked_m out of contract */
+} fgf8_status;
+
+typedef enum { FGF8_F16 = 0, FGF8_BF16 = 1 } fgf8_dtype;
+typedef enum { FGF8_SCALE_F32 = 0, FGF8_SCALE_UE8M0 = 1 } fgf8_scale_fmt;
+
+/*
+ * quantize_1x128 -- activation quantization, 1x128 groups ([DG] "fine-grained
+ * quantization": one scale per token per 128 channels, computed online from the
+ * group's max |x|).
+ *   X   : bf16 [M][K]              input
+ *   Xq  : uint8 [M][K]             E4M3 codes (output)
+ *   SFA : activation scale table for M rows in format fmt (output; layout above)
+ * Requires K % 128 == 0, M >= 0.
+ */
+FGF8_API int quantize_1x128(const void* X, void* Xq, void* SFA, int M, int K, int fmt, void* stream);
+
+/*
+ * quantize_128x128 -- weight quantization, 128x128 blocks per expert ([DG]
+ * "fine-grained quantization": one scale per 128 input x 128 output channels).
+ *   W   : bf16 [G][N][K]           input
+ *   Wq  : uint8 [G][N][K]          E4M3 codes (output)
+ *   SFB : weight scale table (output; layout above)
+ * Requires K % 128 == 0, G >= 1, N >= 1.  A partial last block along N takes
+ * its max over its valid rows.
+ */
+FGF8_API int quantize_128x128(const void* W, void* Wq, void* SFB, int G, int N, int K, int fmt,
+                     void* stream);
+
+/*
+ * gemm_f16 -- dense 16-bit NT GEMM, D[M][N] = A[M][K] * B[N][K]^T, FP32
+ * accumulation, 16-bit output rounded to nearest even ([TIRx] Step 7/8: the
+ * persistent warp-specialised fp16 GEMM; [TC5] section 3: kind::f16 MMA).
+ *   A, B : fp16 or bf16 (in_dtype), D : fp16 or bf16 (out_dtype)
+ * Requires K % 8 == 0, N % 8 == 0, M >= 0, N, K >= 1.
+ */
+FGF8_API int gemm_f16(const void* A, const void* B, void* D, int M, int N, int K, int in_dtype,
+             int out_dtype, void* stream);
+
+/*
+ * gemm_fp8_blockscaled -- dense E4M3 NT GEMM with fine-grained scales:
+ *   D[m,n] = sum_kb SFA(m,kb) * SFB(n,kb) * sum_{k in kb} Aq[m,k] * Bq[n,k]
+ * ([TC5] section 6 block-scaling formula with scale-vector length 128 along K;
+ * [DG] main loop: per-128-K promotion).  FP32 scales run as FP32 partials per
+ * K block promoted on the CUDA cores; UE8M0 scales run on the block-scaled MMA.
+ *   Aq : uint8 [M][K], SFA : activation table (M rows), Bq : uint8 [N][K],
+ *   SFB : weight table (G = 1), D : bf16 [M][N]
+ * Requires K % 128 == 0, N % 8 == 0.
+ */
+FGF8_API int gemm_fp8_blockscaled(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                         void* D, int M, int N, int K, int fmt, void* stream);
+
+/*
+ * grouped_fp8_contiguous -- MoE grouped GEMM, contiguous layout ([DG] "two
+ * grouped layouts": the tokens of one expert are concatenated along M; N and K
+ * are shared by all experts; every expert segment is padded to a multiple of
+ * fgf8_mk_alignment_for_contiguous() rows).
+ *   Aq : uint8 [M][K] (all segments), SFA : activation table for M rows
+ *   Bq : uint8 [G][N][K], SFB : weight table for G experts
+ *   m_indices : int32 [M] on the device: expert of each row, -1 = padding row
+ *   D : bf16 [M][N]; padding rows are not written.
+ * Each aligned block of rows must hold one expert's rows followed by padding;
+ * a row naming another expert sets FGF8_ERR_DEVICE_INPUT and is not written.
+ * Requires K % 128 == 0, N % 8 == 0, M % alignment == 0, G >= 1.
+ */
+FGF8_API int grouped_fp8_contiguous(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                           const int32_t* m_indices, void* D, int M, int N, int K, int G, int fmt,
+                           void* stream);
+
+/*
+ * grouped_fp8_masked -- MoE grouped GEMM, masked layout ([DG] "two grouped
+ * layouts": each expert owns a fixed slot of Mmax rows and a mask says how many
+ * are valid; only valid rows are computed, so the call needs no host knowledge
+ * of the counts and can be captured in a CUDA graph).
+ *   Aq : uint8 [G][Mmax][K], SFA : per expert an activation table for Mmax rows
+ *        (G tables back to back)
+ *   Bq : uint8 [G][N][K], SFB : weight table for G experts
+ *   masked_m : int32 [G] on the device, valid rows per expert (0..Mmax)
+ *   D : bf16 [G][Mmax][N]; rows >= masked_m[g] are not written.
+ *   expected_m : a hint of the typical masked_m (may be 0); unused at present.
+ * Requires K % 128 == 0, N % 8 == 0, 1 <= G <= 1024.
+ */
+FGF8_API int grouped_fp8_masked(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                       const int32_t* masked_m, void* D, int G, int Mmax, int N, int K,
+                       int expected_m, int fmt, void* stream);
+
+/* Row alignment of expert segments in the contiguous layout (the BLOCK_M of the
+ * kernel; [DG] mentions a query of this name for the contiguous layout). */
+FGF8_API int fgf8_mk_alignment_for_contiguous(void);
+
+/* Bytes of an activation scale table for `rows` rows, or of a weight scale
+ * table for G experts of N rows.  Return -1 on invalid arguments. */
+FGF8_API long long fgf8_sfa_bytes(int rows, int K, int fmt);
+FGF8_API long long fgf8_sfb_bytes(int G, int N, int K, int fmt);
+
+/*
+ * fgf8_check_status -- synchronises `stream`, then reads and clears the status
+ * word of the current device.  Returns FGF8_OK, FGF8_ERR_DEVICE_TIMEOUT,
+ * FGF8_ERR_DEVICE_INPUT or FGF8_ERR_CUDA.  *raw_bits (if not NULL) receives the
+ * raw word (bit 0 timeout, bit 1 input, bits 8-10 the role that timed out).
+ */
+FGF8_API int fgf8_check_status(void* stream, unsigned int* raw_bits);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+FGF8_API const char* fgf8_last_error(void);
+
+/* Upper bound, in milliseconds, on any single pipeline wait inside a kernel
+ * (default 2000; also read from the environment variable FGF8_WAIT_TIMEOUT_MS
+ * at first use).  Returns the previous value. */
+FGF8_API int fgf8_set_wait_timeout_ms(int ms);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+FGF8_API int fgf8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGF8_H */

@@ -1,0 +1,118 @@
+"""GPU parity: dense GEMMs (16-bit and FP8 block-scaled) vs the fp64 oracle."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from fine_grained_fp8_persistent_gb300 import inputs
+from parity import gemm_close, nan_filled, sample_entries, to_dev
+
+pytestmark = pytest.mark.gpu
+FMTS = [0, 1]
+
+
+@pytest.fixture(scope="module")
+def fg():
+    from fine_grained_fp8_persistent_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+@functools.lru_cache(maxsize=8)
+def _fp8_case(M, N, K, fmt, seed):
+    import oracle
+    x = inputs.normal_bf16((M, K), seed, outliers=True).float().numpy()
+    w = inputs.normal_bf16((N, K), seed + 1, outliers=True).float().numpy()
+    aq, sfa = oracle.quantize_1x128(x, fmt)
+    bq, sfb = oracle.quantize_128x128(w, fmt)
+    return aq, sfa, bq, sfb
+
+
+def _run_fp8(fg, dev, case, fmt, M, N):
+    aq, sfa, bq, sfb = case
+    out = nan_filled((M, N), dev)
+    fg.gemm_fp8_blockscaled(to_dev(aq, dev), to_dev(sfa, dev), to_dev(bq, dev), to_dev(sfb, dev),
+                            fmt, out=out)
+    rc, bits = fg.check_status()
+    assert rc == 0, (rc, hex(bits), fg.last_error())
+    return out
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 264, 384), (1, 32, 128), (129, 96, 128),
+                                   (256, 512, 1024), (300, 1024, 640)])
+def test_fp8_dense_small(fg, dev, oracle, fmt, M, N, K):
+    case = _fp8_case(M, N, K, fmt, 100 + M + N + K)
+    out = _run_fp8(fg, dev, case, fmt, M, N)
+    ref = oracle.gemm_fp8(*case, fmt)
+    gemm_close(out.float().cpu().numpy(), ref, f"fp8 {M}x{N}x{K} fmt{fmt}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [64, 4096])
+def test_fp8_dense_full_size_sampled(fg, dev, oracle, fmt, M):
+    """The 7168 x 7168 weight at M = 64 (decode) and 4096 (prefill): sampled
+    entries against the oracle, plus the whole output finite."""
+    N = K = 7168
+    case = _fp8_case(M, N, K, fmt, 7)
+    out = _run_fp8(fg, dev, case, fmt, M, N)
+    assert bool(torch.isfinite(out.float()).all())
+    r, c = sample_entries(M, N, 1500, seed=M)
+    ref = oracle.gemm_fp8_entries(*case, fmt, r, c)
+    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
+    gemm_close(got, ref, f"fp8 full M={M} fmt{fmt}")
+
+
+def test_fp8_deterministic(fg, dev):
+    case = _fp8_case(256, 512, 1024, 0, 5)
+    outs = [_run_fp8(fg, dev, case, f, 256, 512) for f in (0, 0, 1, 1)]
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[2].view(torch.int16), outs[3].view(torch.int16))
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 264, 136), (1, 8, 8), (300, 512, 1024)])
+def test_f16_small(fg, dev, oracle, dt, M, N, K):
+    a = inputs.uniform_16bit((M, K), M + K, dtype=dt)
+    b = inputs.uniform_16bit((N, K), N + K + 1, dtype=dt)
+    out = fg.gemm_f16(a.to(dev), b.to(dev))
+    rc, _ = fg.check_status()
+    assert rc == 0
+    assert out.dtype == dt
+    ref = oracle.gemm_f16(a.float().numpy(), b.float().numpy())
+    gemm_close(out.float().cpu().numpy(), ref, f"f16 {M}x{N}x{K}")
+
+
+def test_f16_full_size_sampled(fg, dev, oracle):
+    M = N = K = 4096
+    a = inputs.uniform_16bit((M, K), 11)
+    b = inputs.uniform_16bit((N, K), 12)
+    out = fg.gemm_f16(a.to(dev), b.to(dev))
+    rc, _ = fg.check_status()
+    assert rc == 0
+    assert bool(torch.isfinite(out.float()).all())
+    r, c = sample_entries(M, N, 2000, seed=3)
+    ref = oracle.gemm_f16_entries(a.float().numpy(), b.float().numpy(), r, c)
+    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
+    gemm_close(got, ref, "f16 4096^3")
+
+
+def test_f16_mixed_output_dtype(fg, dev, oracle):
+    a = inputs.uniform_16bit((256, 256), 1)
+    b = inputs.uniform_16bit((256, 256), 2)
+    out = fg.gemm_f16(a.to(dev), b.to(dev), out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_f16(a.float().numpy(), b.float().numpy()))
+
+
+def test_host_validation_errors(fg, dev):
+    a = torch.zeros((16, 100), dtype=torch.uint8, device=dev)
+    with pytest.raises(fg.FGF8Error) as e:
+        fg.gemm_fp8_blockscaled(a, a, a, a, 0)
+    assert e.value.code == 2

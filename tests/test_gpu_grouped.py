@@ -1,0 +1,166 @@
+"""GPU parity: grouped MoE GEMMs (contiguous and masked layouts) vs the oracle."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from fine_grained_fp8_persistent_gb300 import inputs
+from parity import gemm_close, nan_filled, to_dev
+
+pytestmark = pytest.mark.gpu
+FMTS = [0, 1]
+
+
+@pytest.fixture(scope="module")
+def fg():
+    from fine_grained_fp8_persistent_gb300 import binding
+    return binding
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+@functools.lru_cache(maxsize=4)
+def _contig_case(counts, N, K, fmt, seed):
+    import oracle
+    m_idx, M = inputs.contiguous_layout(list(counts), 128)
+    G = len(counts)
+    x = inputs.normal_bf16((M, K), seed, outliers=True).float().numpy()
+    w = inputs.normal_bf16((G, N, K), seed + 1, outliers=True).float().numpy()
+    aq, sfa = oracle.quantize_1x128(x, fmt)
+    bq, sfb = oracle.quantize_128x128(w, fmt)
+    return m_idx.numpy(), aq, sfa, bq, sfb
+
+
+def _run_contig(fg, dev, case, fmt):
+    m_idx, aq, sfa, bq, sfb = case
+    M, N = aq.shape[0], bq.shape[1]
+    out = nan_filled((M, N), dev)
+    fg.grouped_fp8_contiguous(to_dev(aq, dev), to_dev(sfa, dev), to_dev(bq, dev), to_dev(sfb, dev),
+                              to_dev(m_idx, dev), fmt, out=out)
+    return out
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_contiguous_small(fg, dev, oracle, fmt):
+    case = _contig_case((70, 0, 130, 128), 256, 384, fmt, 1)
+    out = _run_contig(fg, dev, case, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    m_idx, aq, sfa, bq, sfb = case
+    ref, valid = oracle.grouped_contiguous(aq, sfa, bq, sfb, m_idx, fmt)
+    o = out.float().cpu().numpy()
+    rows = m_idx >= 0
+    gemm_close(o[rows], ref[rows], "contiguous small")
+    assert np.isnan(o[~rows]).all(), "padding rows were written"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_contiguous_full_size_sampled(fg, dev, oracle, fmt):
+    """8 experts sharing N=4096, K=7168; token counts multinomial(8192, uniform)."""
+    counts = tuple(inputs.expert_counts(8192, 8, seed=0))
+    N, K = 4096, 7168
+    case = _contig_case(counts, N, K, fmt, 3)
+    out = _run_contig(fg, dev, case, fmt)
+    rc, _ = fg.check_status()
+    assert rc == 0
+    m_idx, aq, sfa, bq, sfb = case
+    rng = np.random.default_rng(1)
+    valid_rows = np.flatnonzero(m_idx >= 0)
+    r = rng.choice(valid_rows, 1200)
+    c = rng.integers(0, N, 1200)
+    ref = np.array([oracle.gemm_fp8_entries(aq, sfa, bq[g], sfb[g:g + 1], fmt, [rr], [cc])[0]
+                    for rr, cc, g in zip(r, c, m_idx[r])])
+    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
+    gemm_close(got, ref, "contiguous full")
+    pad = torch.from_numpy(np.flatnonzero(m_idx < 0)).to(dev)
+    assert bool(torch.isnan(out[pad].float()).all())
+    assert bool(torch.isfinite(out[torch.from_numpy(valid_rows).to(dev)].float()).all())
+
+
+def test_contiguous_bad_row_is_reported(fg, dev):
+    case = _contig_case((128, 128), 128, 256, 0, 9)
+    m_idx, aq, sfa, bq, sfb = case
+    bad = m_idx.copy()
+    bad[5] = 1                      # a row of expert 0's block names expert 1
+    out = nan_filled((aq.shape[0], 128), dev)
+    fg.grouped_fp8_contiguous(to_dev(aq, dev), to_dev(sfa, dev), to_dev(bq, dev), to_dev(sfb, dev),
+                              to_dev(bad, dev), 0, out=out)
+    rc, bits = fg.check_status()
+    assert rc == 6 and bits & 2
+    assert bool(torch.isnan(out[5].float()).all())
+
+
+@functools.lru_cache(maxsize=4)
+def _masked_case(G, Mmax, N, K, fmt, seed):
+    import oracle
+    x = inputs.normal_bf16((G, Mmax, K), seed, outliers=True).float().numpy()
+    w = inputs.normal_bf16((G, N, K), seed + 1, outliers=True).float().numpy()
+    qs = [oracle.quantize_1x128(x[g], fmt) for g in range(G)]
+    aq = np.stack([q[0] for q in qs])
+    sfa = np.stack([q[1] for q in qs])
+    bq, sfb = oracle.quantize_128x128(w, fmt)
+    return aq, sfa, bq, sfb
+
+
+def _run_masked(fg, dev, case, masked, fmt):
+    aq, sfa, bq, sfb = case
+    G, Mmax, _ = aq.shape
+    N = bq.shape[1]
+    out = nan_filled((G, Mmax, N), dev)
+    fg.grouped_fp8_masked(to_dev(aq, dev), to_dev(sfa, dev), to_dev(bq, dev), to_dev(sfb, dev),
+                          to_dev(np.asarray(masked, np.int32), dev), fmt, out=out)
+    return out
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("masked", [(0, 256, 17, 1), (128, 129, 255, 0), (0, 0, 0, 0)])
+def test_masked_small(fg, dev, oracle, fmt, masked):
+    case = _masked_case(4, 256, 256, 384, fmt, 2)
+    out = _run_masked(fg, dev, case, masked, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ref, valid = oracle.grouped_masked(*case, np.asarray(masked, np.int32), fmt)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    if v.any():
+        gemm_close(o[v], ref[v], f"masked {masked}")
+    assert np.isnan(o[~v]).all(), "rows beyond masked_m were written"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_masked_full_size_sampled(fg, dev, oracle, fmt):
+    """32 experts, Mmax=256, N=7168, K=2048, valid rows uniform in [0, 256]."""
+    G, Mmax, N, K = 32, 256, 7168, 2048
+    masked = inputs.masked_rows(G, Mmax, seed=0).numpy()
+    case = _masked_case(G, Mmax, N, K, fmt, 4)
+    out = _run_masked(fg, dev, case, masked, fmt)
+    rc, _ = fg.check_status()
+    assert rc == 0
+    aq, sfa, bq, sfb = case
+    rng = np.random.default_rng(2)
+    gs = [g for g in range(G) if masked[g] > 0]
+    g = rng.choice(gs, 1000)
+    m = np.array([rng.integers(0, masked[x]) for x in g])
+    n = rng.integers(0, N, 1000)
+    ref = np.array([oracle.gemm_fp8_entries(aq[gg], sfa[gg], bq[gg], sfb[gg:gg + 1], fmt, [mm], [nn])[0]
+                    for gg, mm, nn in zip(g, m, n)])
+    got = out[torch.from_numpy(g).to(dev), torch.from_numpy(m).to(dev),
+              torch.from_numpy(n).to(dev)].float().cpu().numpy()
+    gemm_close(got, ref, "masked full")
+    rows = torch.arange(Mmax, device=dev)[None, :]
+    vmask = rows < torch.from_numpy(masked).to(dev)[:, None]
+    o = out.float()
+    assert bool(torch.isnan(o[~vmask]).all())
+    assert bool(torch.isfinite(o[vmask]).all())
+
+
+def test_masked_bad_count_is_reported(fg, dev):
+    case = _masked_case(2, 128, 128, 256, 0, 5)
+    out = _run_masked(fg, dev, case, (5, 1000), 0)
+    rc, bits = fg.check_status()
+    assert rc == 6 and bits & 2
