@@ -1,0 +1,438 @@
+"""Benchmark of the fine-grained FP8 GEMM hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  quantize_1x128(X) -> quantize_128x128(W) -> gemm_fp8_blockscaled(UE8M0 scales)
+with X = 4096 x 7168 bf16 activations and W = 7168 x 7168 bf16 weights drawn
+N(0,1) with 1-in-1024 outliers x400 (the FP8 prefill workload: M=4096,
+N=K=7168).  The metric is TFLOPS (2*M*N*K per step / step time) and the GEMM
+kernel's fraction of the GB300 dense FP8 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own batch (weak
+scaling, no collective on the data path); value = all ranks' FLOPs / max time.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_TOK, N_OUT, K_IN = 4096, 7168, 7168
+FLOPS_PER_STEP = 2.0 * M_TOK * N_OUT * K_IN
+WORKLOAD = "fp8 block-scaled NT GEMM M=4096 N=7168 K=7168, UE8M0 scales (quantize 1x128 + 128x128 + GEMM)"
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic of the GEMM kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum per launch), valid only for the kernel sources it was
+# taken from (sha256 over csrc/).  See profiles/.
+NCU_TRAFFIC = {"src_sha": None, "bytes_per_launch": None}
+
+
+def _src_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "fine_grained_fp8_persistent_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ============================================================================ ours
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__ as ge
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world > 1:
+        ge.build()
+    from fine_grained_fp8_persistent_gb300 import binding as fg
+    from fine_grained_fp8_persistent_gb300 import inputs
+
+    UE = fg.SCALE_UE8M0
+    # inputs resident in HBM before the timed region (each rank its own batch)
+    x_cpu = inputs.normal_bf16((M_TOK, K_IN), seed=1000 + rank, outliers=True)
+    w_cpu = inputs.normal_bf16((N_OUT, K_IN), seed=2000, outliers=True)
+    x = x_cpu.to(dev)
+    w = w_cpu.to(dev)
+    xq = torch.empty((M_TOK, K_IN), dtype=torch.uint8, device=dev)
+    wq = torch.empty((N_OUT, K_IN), dtype=torch.uint8, device=dev)
+    sfa_shape, sfa_dt = fg.sfa_shape(M_TOK, K_IN, UE)
+    sfb_shape, sfb_dt = fg.sfb_shape(1, N_OUT, K_IN, UE)
+    sfa = torch.empty(sfa_shape, dtype=sfa_dt, device=dev)
+    sfb = torch.empty(sfb_shape, dtype=sfb_dt, device=dev)
+    d = torch.empty((M_TOK, N_OUT), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fg.quantize_1x128(x, UE, xq, sfa)
+        fg.quantize_128x128(w, UE, wq, sfb)
+        ev_q.record(stream)
+        fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, UE, out=d)
+
+    ev_q = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc, bits = fg.check_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x} after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit()
+                           else local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                     # L2 flush between timed steps (outside the events)
+        starts[i].record(stream)
+        ev_q = mids[i]
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    gemm_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    total_ms = sum(step_ms)
+    rc, bits = fg.check_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits:#x} after the timed steps")
+
+    t_local = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    t_max_ms = float(t_local.item())
+    value = FLOPS_PER_STEP * args.steps * world / (t_max_ms * 1e-3) / 1e12
+
+    e2e = None if args.no_e2e else _e2e(args, fg, x_cpu, w_cpu, dev, stream)
+    variants = _variants(fg, dev, stream) if rank == 0 and not args.no_variants else None
+    cpu = _cpu_baseline(args) if rank == 0 and world == 1 and not args.no_cpu else None
+
+    bf16_peak, bf16_sust, hbm, src = _peaks()
+    fp8_peak = 2.0 * bf16_peak
+    gemm_avg_ms = statistics.mean(gemm_ms)
+    achieved = FLOPS_PER_STEP / (gemm_avg_ms * 1e-3) / 1e12
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["src_sha"] == _src_sha() else None
+    if rank == 0:
+        line = {
+            "metric": "TFLOPS (FP8 block-scaled NT GEMM step, fraction of GB300 dense FP8 tensor peak)",
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(t_max_ms / args.steps, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3 x e4m3 -> f32 accumulate (bf16 out)",
+            "data": "synthetic (seeded N(0,1) bf16, 1/1024 outliers x400)",
+            "config": {"workload": WORKLOAD, "M": M_TOK, "N": N_OUT, "K": K_IN,
+                       "scale_format": "ue8m0", "per_rank_batch_tokens": M_TOK,
+                       "l2": "flushed between steps (256 MiB write outside the timed events)",
+                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+            "gemm_ms": round(gemm_avg_ms, 4),
+            "quantize_ms": round(statistics.mean(s - g for s, g in zip(step_ms, gemm_ms)), 4),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                         "traffic": traffic,
+                         "peak_note": f"FP8 dense = 2 x bf16 burst GEMM peak ({bf16_peak} TFLOP/s, {src}); "
+                                      f"vs sustained: {round(achieved / (2 * bf16_sust), 4)}",
+                         "kernel": "gemm_kernel<MXF8, Dense, 224, 4>"},
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": round(wall, 3),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if variants is not None:
+            line["variants"] = variants
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _e2e(args, fg, x_cpu, w_cpu, dev, stream) -> dict:
+    """Same step through the public API from pinned HOST buffers: H2D of X and W,
+    quantize, GEMM, D2H of the result, every step inside the timed region."""
+    import torch
+    UE = fg.SCALE_UE8M0
+    xh = x_cpu.pin_memory()
+    wh = w_cpu.pin_memory()
+    dh = torch.empty((M_TOK, N_OUT), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(xh, device=dev)
+    wd = torch.empty_like(wh, device=dev)
+    steps = max(3, min(args.steps, 10))
+
+    def one():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        xq, sfa = fg.quantize_1x128(xd, UE)
+        wq, sfb = fg.quantize_128x128(wd, UE)
+        d = fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, UE)
+        dh.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(FLOPS_PER_STEP / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": xh.numel() * 2 + wh.numel() * 2,
+            "d2h_bytes_per_step": dh.numel() * 2}
+
+
+def _variants(fg, dev, stream) -> dict:
+    """Kernel-only throughput of the other GEMM forms on their own workloads."""
+    import torch
+    from fine_grained_fp8_persistent_gb300 import inputs
+    out = {}
+    bf16_peak, _, _, src = _peaks()
+
+    def timeit(fn, iters=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * iters)]
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        tot = 0.0
+        for i in range(iters):
+            flush.zero_()
+            es[2 * i].record(stream)
+            fn()
+            es[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        for i in range(iters):
+            tot += es[2 * i].elapsed_time(es[2 * i + 1])
+        return tot / iters
+
+    x = inputs.normal_bf16((M_TOK, K_IN), 1, outliers=True).to(dev)
+    w = inputs.normal_bf16((N_OUT, K_IN), 2, outliers=True).to(dev)
+    for name, fmt in (("fp8_f32scale_4096x7168x7168", fg.SCALE_F32), ("fp8_ue8m0_64x7168x7168", fg.SCALE_UE8M0)):
+        m = 64 if "64x" in name else M_TOK
+        xq, sfa = fg.quantize_1x128(x[:m].contiguous(), fmt)
+        wq, sfb = fg.quantize_128x128(w, fmt)
+        d = torch.empty((m, N_OUT), dtype=torch.bfloat16, device=dev)
+        ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fmt, out=d))
+        tf = 2.0 * m * N_OUT * K_IN / (ms * 1e-3) / 1e12
+        byts = m * K_IN + N_OUT * K_IN + m * N_OUT * 2
+        out[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                     "frac_fp8_peak": round(tf / (2 * bf16_peak), 4),
+                     "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+    a = inputs.uniform_16bit((4096, 4096), 3).to(dev)
+    b = inputs.uniform_16bit((4096, 4096), 4).to(dev)
+    d16 = torch.empty((4096, 4096), dtype=torch.float16, device=dev)
+    ms = timeit(lambda: fg.gemm_f16(a, b, out=d16))
+    tf = 2.0 * 4096 ** 3 / (ms * 1e-3) / 1e12
+    out["f16_4096x4096x4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                 "frac_bf16_peak": round(tf / bf16_peak, 4)}
+    xb = inputs.normal_bf16((M_TOK, K_IN), 5, outliers=True).to(dev)
+    ms = timeit(lambda: fg.quantize_1x128(xb, fg.SCALE_UE8M0))
+    byts = M_TOK * K_IN * 3 + M_TOK * K_IN // 128
+    out["quantize_1x128_4096x7168"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+    wb = inputs.normal_bf16((N_OUT, K_IN), 6, outliers=True).to(dev)
+    ms = timeit(lambda: fg.quantize_128x128(wb, fg.SCALE_UE8M0))
+    byts = N_OUT * K_IN * 3 + N_OUT * K_IN // 128
+    out["quantize_128x128_7168x7168"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+    return out
+
+
+# ============================================================================ oracle (CPU)
+def _oracle_sample(rows: int):
+    """One bounded sample of the workload on the CPU oracle: quantize `rows`
+    activation rows (1x128) and the whole weight (128x128), then compute those
+    rows of D.  Returns (seconds, FLOPs of the GEMM part)."""
+    import numpy as np
+    import oracle
+    from fine_grained_fp8_persistent_gb300 import inputs
+    x = inputs.normal_bf16((rows, K_IN), seed=1000, outliers=True).float().numpy()
+    w = inputs.normal_bf16((N_OUT, K_IN), seed=2000, outliers=True).float().numpy()
+    t0 = time.perf_counter()
+    aq, sfa = oracle.quantize_1x128(x, oracle.SCALE_UE8M0)
+    bq, sfb = oracle.quantize_128x128(w, oracle.SCALE_UE8M0)
+    oracle.gemm_fp8(aq, sfa, bq, sfb, oracle.SCALE_UE8M0)
+    return time.perf_counter() - t0, 2.0 * rows * N_OUT * K_IN
+
+
+def _cpu_baseline(args) -> dict:
+    import oracle
+    oracle.build()
+    rows = args.cpu_rows
+    secs, flops = _oracle_sample(rows)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{rows} of {M_TOK} output rows: quantize {rows}x{K_IN} (1x128) + "
+                      f"{N_OUT}x{K_IN} (128x128) + GEMM {rows}x{N_OUT}x{K_IN}, UE8M0, fp64 oracle",
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args) -> None:
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    rows = args.cpu_rows
+    for _ in range(args.warmup):
+        _oracle_sample(rows)
+    tot = 0.0
+    flops = 0.0
+    for _ in range(args.steps):
+        s, f = _oracle_sample(rows)
+        tot += s
+        flops += f
+    value = flops / tot / 1e12
+    cores = oracle.num_threads()
+    sample = (f"{rows} of {M_TOK} output rows per step: quantize {rows}x{K_IN} (1x128) + "
+              f"{N_OUT}x{K_IN} (128x128) + GEMM {rows}x{N_OUT}x{K_IN}, UE8M0, fp64 oracle")
+    line = {
+        "impl": "reference",
+        "metric": "TFLOPS (FP8 block-scaled NT GEMM step, fraction of GB300 dense FP8 tensor peak)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 codes, f64 accumulate", "data": "synthetic (seeded N(0,1) bf16, 1/1024 outliers x400)",
+        "config": {"workload": WORKLOAD, "M": M_TOK, "N": N_OUT, "K": K_IN, "scale_format": "ue8m0",
+                   "parallelism": "CPU oracle on the host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=8, help="output rows in one oracle sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--no-variants", action="store_true", help="skip the extra kernel lines")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

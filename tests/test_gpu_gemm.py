@@ -69,11 +69,12 @@ def test_fp8_dense_full_size_sampled(fg, dev, oracle, fmt, M):
     gemm_close(got, ref, f"fp8 full M={M} fmt{fmt}")
 
 
-def test_fp8_deterministic(fg, dev):
-    case = _fp8_case(256, 512, 1024, 0, 5)
-    outs = [_run_fp8(fg, dev, case, f, 256, 512) for f in (0, 0, 1, 1)]
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp8_deterministic(fg, dev, fmt):
+    case = _fp8_case(256, 512, 1024, fmt, 5)
+    outs = [_run_fp8(fg, dev, case, fmt, 256, 512) for _ in range(3)]
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
-    assert torch.equal(outs[2].view(torch.int16), outs[3].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
 
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
