@@ -6,11 +6,15 @@ namespace fgf8 {
 namespace {
 
 template <Sched S>
-int launch_bn(int bn, const GemmArgs& a, const TensorMaps& tm, int grid, cudaStream_t stream) {
-  switch (bn) {
-    case 256: return launch_instance<Kind::F8F32, S, 256, 4>(a, tm, grid, stream);
-    case 128: return launch_instance<Kind::F8F32, S, 128, 6>(a, tm, grid, stream);
-    default: return launch_instance<Kind::F8F32, S, 64, 8>(a, tm, grid, stream);
+int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
+               cudaStream_t stream) {
+  if constexpr (S != Sched::Contiguous) {
+    if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 256, 6>(a, tm, tiles, stream);
+  }
+  switch (c.bn) {
+    case 256: return launch_persistent<Kind::F8F32, S, 1, 256, 4>(a, tm, tiles, stream);
+    case 128: return launch_persistent<Kind::F8F32, S, 1, 128, 6>(a, tm, tiles, stream);
+    default: return launch_persistent<Kind::F8F32, S, 1, 64, 8>(a, tm, tiles, stream);
   }
 }
 
@@ -18,18 +22,22 @@ int launch_bn(int bn, const GemmArgs& a, const TensorMaps& tm, int grid, cudaStr
 
 int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
                       cudaStream_t stream) {
-  static const int cands[] = {256, 128, 64};
-  const int bn = pick_bn(a, sched, cands, 3);
+  static const TileCfg pair_cands[] = {{2, 256}, {1, 256}, {1, 128}, {1, 64}};
+  static const TileCfg single_cands[] = {{1, 256}, {1, 128}, {1, 64}};
+  const bool pairs = sched != Sched::Contiguous;
+  const TileCfg* cands = pairs ? pair_cands : single_cands;
+  const int n = pairs ? 4 : 3;
+  const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
   TensorMaps tm;
-  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, bn))
+  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta))
     return 4;
-  const int grid = persistent_grid(tile_count(a, sched, bn));
+  const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_bn<Sched::Dense>(bn, a, tm, grid, stream);
-    case Sched::Contiguous: return launch_bn<Sched::Contiguous>(bn, a, tm, grid, stream);
-    default: return launch_bn<Sched::Masked>(bn, a, tm, grid, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, stream);
+    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, stream);
   }
 }
 

@@ -1,78 +1,112 @@
-// gemm_launch.cuh -- host-side launch of one GEMM kernel instantiation, tensor-map
-// set-up and the tile-shape heuristic shared by the launcher translation units.
+// gemm_launch.cuh -- host side of one GEMM launch: tensor maps, the tile-shape
+// heuristic, persistent grid sizing and the cluster launch.
 #pragma once
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
-#include "gemm_kernel.cuh"
+#include "gemm_persistent.cuh"
 
 namespace fgf8 {
 
-// Persistent grid: one CTA per SM (the SMEM footprint keeps it at one), never
-// more CTAs than tiles.
-inline int persistent_grid(long long tiles) {
-  const long long sms = device_sm_count();
-  if (tiles <= 0) return 1;
-  return static_cast<int>(tiles < sms ? tiles : sms);
-}
+// One kernel configuration the launchers can choose from.
+struct TileCfg {
+  int ncta;   // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
+  int bn;     // tile width
+};
 
-template <Kind KIND, Sched SCHED, int BN, int STAGES>
-int launch_instance(const GemmArgs& a, const TensorMaps& tm, int grid, cudaStream_t stream) {
-  using C = GemmCfg<KIND, SCHED, BN, STAGES>;
-  auto* fn = &gemm_kernel<KIND, SCHED, BN, STAGES>;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (C::SMEM_BYTES > device_max_smem_optin())
-    return set_error(2, "tile %dx%d needs %d bytes of shared memory", C::BM, BN, C::SMEM_BYTES);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return set_error(4, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured[dev] = true;
-  }
-  fn<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tm.a, tm.b, tm.sfa, tm.sfb, a);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
-  return 0;
-}
-
-// Tiles of the problem for a given BN (masked: the upper bound with every expert full).
-inline long long tile_count(const GemmArgs& a, Sched s, int bn) {
-  const long long mt = (a.M + 127) / 128;
-  const long long nt = (a.N + bn - 1) / bn;
+// Tiles of the problem for a configuration (masked: upper bound, every expert full).
+inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
+  const long long tm = 128LL * c.ncta;
+  const long long mt = (a.M + tm - 1) / tm;
+  const long long nt = (a.N + c.bn - 1) / c.bn;
   return (s == Sched::Masked ? a.G : 1) * mt * nt;
 }
 
-// Pick the widest tile that does not cost extra waves: estimated time is
-// waves * (BN + 32), where 32 stands for the per-tile cost that does not scale
-// with BN (the A tile, the epilogue drain).  Wide tiles make the MMA and the
-// B traffic per output cheaper; narrow tiles spread a skinny problem over more
-// SMs (the DeepGEMM page's unaligned-BLOCK_N argument: 112 vs 128 blocks on 132
-// SMs).
-inline int pick_bn(const GemmArgs& a, Sched s, const int* cands, int n) {
+// Estimated time of a configuration: waves of tiles over the SMs times the
+// per-tile cost (BN + 32: the 32 stands for the work that does not scale with
+// BN: the A tile, the epilogue drain).  A pair tile computes twice the rows on
+// two SMs with half the B traffic per SM; it is credited 10 % for that.  Narrow
+// tiles spread skinny problems over more SMs (the DeepGEMM page's unaligned
+// BLOCK_N argument: 112 vs 128 blocks on 132 SMs).
+// FGF8_FORCE_TILE="<ncta>x<bn>" (e.g. "2x224") selects that configuration when it
+// is among the candidates (used by the tests to cover every instantiation).
+inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
+  if (const char* f = std::getenv("FGF8_FORCE_TILE")) {
+    int nc = 0, bn = 0;
+    if (std::sscanf(f, "%dx%d", &nc, &bn) == 2)
+      for (int i = 0; i < n; ++i)
+        if (cands[i].ncta == nc && cands[i].bn == bn) return i;
+  }
   const long long sms = device_sm_count();
-  int best = cands[0];
-  long long best_cost = -1;
+  int best = 0;
+  double best_cost = -1.0;
   for (int i = 0; i < n; ++i) {
-    const long long tiles = tile_count(a, s, cands[i]);
-    const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (cands[i] + 32);
+    const long long units = sms / cands[i].ncta;
+    const long long waves = (tile_count(a, s, cands[i]) + units - 1) / units;
+    const double cost = static_cast<double>(waves) * (cands[i].bn + 32) * (cands[i].ncta == 2 ? 0.9 : 1.0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = cands[i];
+      best = i;
     }
   }
   return best;
 }
 
-// A and B operand maps: K-major rows of 128 bytes per stage, 128-byte swizzle.
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES>
+int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES>;
+  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES>;
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return set_error(2, "device id %d", dev);
+  if (C::SMEM_BYTES > device_max_smem_optin())
+    return set_error(2, "tile needs %d bytes of shared memory", C::SMEM_BYTES);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = NCTA;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return set_error(4, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    int clusters = 0;
+    cfg.gridDim = dim3(NCTA * device_sm_count(), 1, 1);
+    // the CTAs of a cluster are co-scheduled inside one GPC, so the number of pairs
+    // that fit can be below SMs / 2 ("Dissecting NVIDIA Blackwell" (EEPW), section
+    // on clusters, GPCs and die yield)
+    e = NCTA == 2 ? cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) : cudaSuccess;
+    if (NCTA == 1) clusters = device_sm_count();
+    if (e != cudaSuccess || clusters <= 0)
+      return set_error(4, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+    max_clusters[dev] = clusters;
+  }
+  long long clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * NCTA), 1, 1);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, a);
+  if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+// A and B operand maps: K-major rows of 128 bytes per stage, 128-byte swizzle;
+// each CTA loads 128 rows of A and BN / NCTA rows of B.
 inline int make_operand_maps(TensorMaps& tm, CUtensorMapDataType dt, int elem_bytes, const void* A,
-                             long long a_rows, const void* B, long long b_rows, int K, int bn) {
+                             long long a_rows, const void* B, long long b_rows, int K, int b_box_rows) {
   std::memset(&tm, 0, sizeof(tm));
   const uint32_t bk = 128 / elem_bytes;
   if (!encode_tmap_2d(&tm.a, dt, A, K, a_rows, static_cast<uint64_t>(K) * elem_bytes, bk, 128, true))
     return 4;
-  if (!encode_tmap_2d(&tm.b, dt, B, K, b_rows, static_cast<uint64_t>(K) * elem_bytes, bk, bn, true))
+  if (!encode_tmap_2d(&tm.b, dt, B, K, b_rows, static_cast<uint64_t>(K) * elem_bytes, bk, b_box_rows,
+                      true))
     return 4;
   return 0;
 }

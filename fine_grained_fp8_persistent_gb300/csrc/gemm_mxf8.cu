@@ -6,12 +6,19 @@ namespace fgf8 {
 namespace {
 
 template <Sched S>
-int launch_bn(int bn, const GemmArgs& a, const TensorMaps& tm, int grid, cudaStream_t stream) {
-  switch (bn) {
-    case 224: return launch_instance<Kind::MXF8, S, 224, 4>(a, tm, grid, stream);
-    case 128: return launch_instance<Kind::MXF8, S, 128, 6>(a, tm, grid, stream);
-    case 64: return launch_instance<Kind::MXF8, S, 64, 8>(a, tm, grid, stream);
-    default: return launch_instance<Kind::MXF8, S, 32, 8>(a, tm, grid, stream);
+int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
+               cudaStream_t stream) {
+  if constexpr (S != Sched::Contiguous) {
+    if (c.ncta == 2) {
+      if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 6>(a, tm, tiles, stream);
+      return launch_persistent<Kind::MXF8, S, 2, 128, 8>(a, tm, tiles, stream);
+    }
+  }
+  switch (c.bn) {
+    case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 4>(a, tm, tiles, stream);
+    case 128: return launch_persistent<Kind::MXF8, S, 1, 128, 6>(a, tm, tiles, stream);
+    case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 8>(a, tm, tiles, stream);
+    default: return launch_persistent<Kind::MXF8, S, 1, 32, 8>(a, tm, tiles, stream);
   }
 }
 
@@ -19,29 +26,32 @@ int launch_bn(int bn, const GemmArgs& a, const TensorMaps& tm, int grid, cudaStr
 
 int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
                      const void* Bq, const void* SFB, cudaStream_t stream) {
-  static const int cands[] = {224, 128, 64, 32};
-  const int bn = pick_bn(a, sched, cands, 4);
+  // the contiguous layout aligns expert segments to 128 rows: one CTA per tile
+  static const TileCfg pair_cands[] = {{2, 224}, {2, 128}, {1, 224}, {1, 128}, {1, 64}, {1, 32}};
+  static const TileCfg single_cands[] = {{1, 224}, {1, 128}, {1, 64}, {1, 32}};
+  const bool pairs = sched != Sched::Contiguous;
+  const TileCfg* cands = pairs ? pair_cands : single_cands;
+  const int n = pairs ? 6 : 4;
+  const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
   TensorMaps tm;
-  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, bn))
+  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta))
     return 4;
   // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
   const long long kq = (a.K / 128 + 3) / 4;
   const long long lda = (a.M + 3) / 4 * 4;
   const long long ldn = (a.N + 3) / 4 * 4;
   const long long sfa_rows = kq * (sched == Sched::Masked ? a.G : 1);
-  if (!encode_tmap_2d(&tm.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFA, lda, sfa_rows, lda * 4, 128, 1,
-                      false))
+  if (!encode_tmap_2d(&tm.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFA, lda, sfa_rows, lda * 4, 128, 1, false))
     return 4;
-  if (!encode_tmap_2d(&tm.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, ldn, kq * a.G, ldn * 4, bn, 1,
-                      false))
+  if (!encode_tmap_2d(&tm.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, ldn, kq * a.G, ldn * 4, c.bn, 1, false))
     return 4;
-  const int grid = persistent_grid(tile_count(a, sched, bn));
+  const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_bn<Sched::Dense>(bn, a, tm, grid, stream);
-    case Sched::Contiguous: return launch_bn<Sched::Contiguous>(bn, a, tm, grid, stream);
-    default: return launch_bn<Sched::Masked>(bn, a, tm, grid, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, stream);
+    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, stream);
   }
 }
 

@@ -1,0 +1,697 @@
+// gemm_persistent.cuh -- persistent, warp-specialised NT GEMM for sm_103a, on one
+// CTA or on a CTA pair (cta_group::2).
+//
+//   D[M,N] = A[M,K] * B[N,K]^T, FP32 accumulation, 16-bit output.
+//
+// A tile is (128 * NCTA) rows x BN columns.  With NCTA = 2 the two CTAs of a
+// cluster form a pair: each holds its own 128 rows of A and half of the BN rows
+// of B; one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = 256,
+// and each CTA's TMEM receives its own 128 accumulator rows ("GPU GEMM part 4:
+// tcgen05 & Blackwell", section 5.2: A and D split along M, B along N; "Blackwell
+// Tensor Core: tcgen05.mma", cta_group::2 M = 256 layout).  Halving each CTA's B
+// tile cuts both its SMEM footprint and its L2->SMEM traffic per FLOP by a third,
+// which leaves room for a deeper pipeline.
+//
+// Roles (per CTA):
+//   warp 0   TMA producer: A/B tiles into a STAGES-deep ring of 128-byte-swizzled
+//            stages.  In a pair both CTAs' loads complete on the even CTA's `full`
+//            barrier (cp.async.bulk.tensor .cta_group::2).
+//   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).
+//   warp 2   (UE8M0 kernels) scale-word transposer: after a stage's packed scale
+//            words land, rearranges them into the 32 x 128-bit layout tcgen05.cp
+//            copies and tells the MMA issuer (`sf_ready`, counted over the pair).
+//   rest     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
+//            promotion (8 warps: per-128-K partial from TMEM, acc += sA*sB*partial
+//            on the CUDA cores, the DeepGEMM page's promotion loop).
+// Pipeline handshakes follow the tma2mma / mma2tma / mma2ld / ld2mma barriers of
+// "TIRx and high-performance GEMM (part 2)" (Steps 7-8); every wait is bounded.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+
+namespace fgf8 {
+
+// ----------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+template <int NCTA>
+__device__ __forceinline__ void tma_load_ab(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                            int32_t x, int32_t y) {
+  if constexpr (NCTA == 2) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+  } else {
+    ptx::tma_load_2d(dst, m, bar_cluster, x, y);
+  }
+}
+
+// tcgen05 ops with the kernel-wide cta_group.
+template <int NCTA>
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  if constexpr (NCTA == 2)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+  else
+    ptx::mma_commit(bar);
+}
+// Arrive on `bar` in every CTA of the pair once the tracked ops complete.
+template <int NCTA>
+__device__ __forceinline__ void tc_commit_all(uint32_t bar) {
+  if constexpr (NCTA == 2)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+  else
+    ptx::mma_commit(bar);
+}
+template <int NCTA>
+__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
+  if constexpr (NCTA == 2) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    ptx::tmem_alloc(dst_smem, ncols);
+    ptx::tmem_relinquish();
+  }
+}
+template <int NCTA>
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  if constexpr (NCTA == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    ptx::tmem_dealloc(taddr, ncols);
+}
+template <int NCTA>
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  if constexpr (NCTA == 2)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+  else
+    ptx::tmem_cp_32x128b_warpx4(taddr, sdesc);
+}
+template <int NCTA, Kind KIND>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  if constexpr (NCTA == 2) {
+    if constexpr (KIND == Kind::MXF8)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+          " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+          "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+          : "memory");
+    else if constexpr (KIND == Kind::F8F32)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+          "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+          "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+          : "memory");
+  } else {
+    if constexpr (KIND == Kind::MXF8) ptx::mma_mxf8(d, ad, bd, idesc, sfa, sfb, acc);
+    else if constexpr (KIND == Kind::F8F32) ptx::mma_f8(d, ad, bd, idesc, acc);
+    else ptx::mma_f16(d, ad, bd, idesc, acc);
+  }
+}
+
+// Bounded wait with cluster-scope acquire (barriers that receive the peer's arrivals).
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct PairWaitCtl {
+  volatile uint32_t* abort_flag;   // this CTA's flag (shared memory)
+  uint32_t peer_abort;             // the peer's flag (cluster address), 0 if none
+  uint32_t* status;
+  uint64_t timeout_ns;
+  uint32_t role_bit;
+};
+
+__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairWaitCtl& c) {
+  bool ok = try_wait_cluster(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+      if (try_wait_cluster(bar, parity)) { ok = true; break; }
+      if ((i & 63u) == 0) {
+        if (*c.abort_flag) break;
+        if (ptx::globaltimer() - t0 > c.timeout_ns) {
+          *c.abort_flag = 1u;
+          if (c.peer_abort) st_cluster_u32(c.peer_abort, 1u);
+          atomicOr(c.status, FGF8_DEVERR_TIMEOUT | c.role_bit);
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_>
+struct PCfg {
+  static constexpr int NCTA = NCTA_;
+  static constexpr int BM = 128;                    // rows per CTA
+  static constexpr int TILE_M = BM * NCTA;
+  static constexpr int BN = BN_;
+  static constexpr int BN_LOCAL = BN / NCTA;        // B rows held by each CTA
+  static constexpr int STAGES = STAGES_;
+  static_assert(NCTA == 1 || NCTA == 2, "one CTA or a pair");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(BN_LOCAL % 16 == 0, "B rows per CTA");
+  static constexpr bool kMX = KIND == Kind::MXF8;
+  static constexpr bool kF32S = KIND == Kind::F8F32;
+  static constexpr int BK = (KIND == Kind::F16) ? 64 : 128;
+  static constexpr int MMA_K_BYTES = 32;
+  static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN_LOCAL * 128;
+  static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
+  static constexpr int SFA_BYTES = kMX ? BM * 4 : 0;
+  static constexpr int SFB_BYTES = kMX ? SFB_ROWS * 4 : 0;
+  static constexpr int SF_WARPS = kMX ? 1 : 0;
+  static constexpr int EPI_WARPS = kF32S ? 8 : 4;
+  static constexpr int EPI_WARP0 = 2 + SF_WARPS;
+  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr int MAX_GROUPS = 1024;
+
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_BAR = (OFF_SFB + STAGES * SFB_BYTES + 7) / 8 * 8;
+  static constexpr int BAR_FULL = 0;
+  static constexpr int BAR_EMPTY = STAGES;
+  static constexpr int BAR_SFL = 2 * STAGES;        // scale words landed (local)
+  static constexpr int BAR_SFR = 3 * STAGES;        // scale words transposed (even CTA, pair count)
+  static constexpr int BAR_ACC_FULL = 4 * STAGES;   // 2
+  static constexpr int BAR_ACC_EMPTY = 4 * STAGES + 2;
+  static constexpr int BAR_SF_FREE = 4 * STAGES + 4;
+  static constexpr int BAR_DRAIN = 4 * STAGES + 6;
+  static constexpr int NUM_BARS = 4 * STAGES + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
+  static constexpr int PREFIX_BYTES = (SCHED == Sched::Masked) ? (MAX_GROUPS + 1) * 4 : 0;
+  static constexpr int SMEM_BYTES = OFF_PREFIX + PREFIX_BYTES + 1024;
+
+  static constexpr int ACC_COLS = 2 * BN;
+  static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
+  static constexpr int SF_COL0 = ACC_COLS;
+  static constexpr int TMEM_USED = ACC_COLS + (kMX ? 2 * SF_SLOT_COLS : 0);
+  static constexpr int TMEM_ALLOC = TMEM_USED <= 32    ? 32
+                                    : TMEM_USED <= 64  ? 64
+                                    : TMEM_USED <= 128 ? 128
+                                    : TMEM_USED <= 256 ? 256
+                                                       : 512;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
+  static constexpr uint32_t SF_TX = BM * 4 + BN * 4;             // bytes landing on `sf_loaded`
+};
+
+// Rearranges 128 packed scale words (row-major over 128 rows) in place so that
+// row 32 j + l sits at word 4 l + j: TMEM lane l, column j after tcgen05.cp.
+__device__ __forceinline__ void sf_transpose(uint32_t* p, uint32_t lane) {
+  const uint32_t v0 = p[lane], v1 = p[32 + lane], v2 = p[64 + lane], v3 = p[96 + lane];
+  __syncwarp();
+  *reinterpret_cast<uint4*>(p + 4 * lane) = make_uint4(v0, v1, v2, v3);
+  __syncwarp();
+}
+
+__device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 32 consecutive FP32 values of one output row -> 16-bit, columns col0..col0+31
+// clipped at N (N is a multiple of 8).
+__device__ __forceinline__ void store_row32(void* D, size_t row_off, int col0, int N,
+                                            const float* v, bool bf16) {
+  uint16_t* out = reinterpret_cast<uint16_t*>(D) + row_off;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int col = col0 + 8 * j;
+    if (col < N) {
+      uint4 w;
+      w.x = pack_2x16(v[8 * j + 0], v[8 * j + 1], bf16);
+      w.y = pack_2x16(v[8 * j + 2], v[8 * j + 3], bf16);
+      w.z = pack_2x16(v[8 * j + 4], v[8 * j + 5], bf16);
+      w.w = pack_2x16(v[8 * j + 6], v[8 * j + 7], bf16);
+      *reinterpret_cast<uint4*>(out + col) = w;
+    }
+  }
+}
+
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 1)
+    gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_sfa,
+                    const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t lane = threadIdx.x % 32;
+  const uint32_t rank = (NCTA == 2) ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
+  // the even CTA's copy of barrier i (cluster address)
+  auto lbar = [&](int i) -> uint32_t { return NCTA == 2 ? map_to_rank(bar(i), 0) : bar(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
+
+  const int M = args.M, N = args.N, K = args.K, G = args.G;
+  const int nkb = (K + C::BK - 1) / C::BK;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_m = (M + C::TILE_M - 1) / C::TILE_M;   // per expert for masked
+  const int kq = (K / 128 + 3) / 4;
+  const int cluster_id = static_cast<int>(blockIdx.x) / NCTA;
+  const int num_clusters = static_cast<int>(gridDim.x) / NCTA;
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(C::BAR_FULL + s), 1);
+      ptx::mbar_init(bar(C::BAR_EMPTY + s), 1);
+      ptx::mbar_init(bar(C::BAR_SFL + s), 1);
+      ptx::mbar_init(bar(C::BAR_SFR + s), NCTA);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
+      ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
+      ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
+    }
+    ptx::mbar_init(bar(C::BAR_DRAIN), 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if constexpr (SCHED == Sched::Masked) {
+    if (warp == 2) {
+      int run = 0;
+      for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + static_cast<int>(lane);
+        int mm = (g < G) ? args.masked_m[g] : 0;
+        if (mm < 0 || mm > M) {
+          if (leader) atomicOr(args.status, FGF8_DEVERR_INPUT);
+          mm = mm < 0 ? 0 : M;
+        }
+        int v = (mm + C::TILE_M - 1) / C::TILE_M * num_n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, v, off);
+          if (static_cast<int>(lane) >= off) v += o;
+        }
+        if (g < G) prefix[g + 1] = run + v;
+        run += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) prefix[0] = 0;
+    }
+  }
+  if (warp == 1) {
+    tc_alloc<NCTA>(ptx::smem_u32(tmem_slot), C::TMEM_ALLOC);
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  if constexpr (NCTA == 2) cluster_sync_all();   // peer barriers initialised before any remote use
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int num_tiles;
+  if constexpr (SCHED == Sched::Masked) num_tiles = prefix[G];
+  else num_tiles = num_m * num_n;
+
+  auto get_tile = [&](int t, Tile& tl) -> bool {
+    int m, n, g = 0, rows;
+    if constexpr (SCHED == Sched::Masked) {
+      int lo = 0, hi = G - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      g = lo;
+      int mm = __ldg(args.masked_m + g);
+      rows = mm < 0 ? 0 : (mm > M ? M : mm);
+      const int mt = (rows + C::TILE_M - 1) / C::TILE_M;
+      const int local = t - prefix[g];
+      n = local / mt;                              // M blocks sharing a B tile are adjacent
+      m = local - n * mt;
+    } else {
+      dense_tile(t, num_m, num_n, 16, m, n);
+      rows = M;
+      if constexpr (SCHED == Sched::Contiguous) {
+        g = __ldg(args.m_indices + m * C::TILE_M);
+        if (g < 0 || g >= G) return false;
+      }
+    }
+    const int m_in_expert = m * C::TILE_M + static_cast<int>(rank) * C::BM;
+    tl.m_blk = m_in_expert;                       // first row of this CTA within the expert
+    tl.n_blk = n;
+    tl.group = g;
+    tl.a_row0 = (SCHED == Sched::Masked ? g * M : 0) + m_in_expert;
+    tl.b_row0 = (SCHED == Sched::Dense ? 0 : g * N) + n * BN + static_cast<int>(rank) * C::BN_LOCAL;
+    tl.row_limit = rows - m_in_expert;
+    return true;
+  };
+
+  PairWaitCtl ctl{abort_flag,
+                  NCTA == 2 ? map_to_rank(sbase + C::OFF_MISC + 4, rank ^ 1u) : 0u,
+                  args.status, args.timeout_ns, 0};
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_a);
+      ptx::prefetch_tmap(&tm_b);
+      if constexpr (C::kMX) {
+        ptx::prefetch_tmap(&tm_sfa);
+        ptx::prefetch_tmap(&tm_sfb);
+      }
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+      Tile tl;
+      if (!get_tile(t, tl)) continue;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!pwait(bar(C::BAR_EMPTY + stage), phase ^ 1u, ctl)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t full = lbar(C::BAR_FULL + stage);
+          if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
+          tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
+          tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
+          if (C::kMX && kb % 4 == 0) {
+            const uint32_t sfl = bar(C::BAR_SFL + stage);
+            ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
+            const int sfa_row = (SCHED == Sched::Masked ? tl.group * kq : 0) + kb / 4;
+            ptx::tma_load_2d(sbase + C::OFF_SFA + stage * C::SFA_BYTES, &tm_sfa, sfl, tl.m_blk, sfa_row);
+            ptx::tma_load_2d(sbase + C::OFF_SFB + stage * C::SFB_BYTES, &tm_sfb, sfl, tl.n_blk * BN,
+                             tl.group * kq + kb / 4);
+          }
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    aborted = !ok;
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0, sfr_bits = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      uint32_t sf_uses0 = 0u, sf_uses1 = 0u, gctr = 0u;
+      bool ok = true;
+      const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
+      const uint32_t idesc_plain = idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
+      for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+        Tile tl;
+        if (!get_tile(t, tl)) continue;
+        if constexpr (!C::kF32S) {
+          if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
+        }
+        uint32_t slot = 0;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!pwait(bar(C::BAR_FULL + stage), phase, ctl)) { ok = false; break; }
+          if constexpr (C::kF32S) {
+            if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
+          }
+          const bool sf_block = C::kMX && (kb % 4 == 0);
+          if (sf_block) {
+            slot = gctr & 1u;
+            const uint32_t uses = slot ? sf_uses1 : sf_uses0;
+            if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
+            if (!pwait(bar(C::BAR_SFR + stage), (sfr_bits >> stage) & 1u, ctl)) { ok = false; break; }
+            sfr_bits ^= 1u << stage;
+          }
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+            if (sf_block) {
+              const uint32_t sfa = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
+              const uint32_t sfb = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+              tc_cp_sf<NCTA>(sf_col, smem_desc_plain_rows16(sfa));
+#pragma unroll
+              for (int c = 0; c < C::SFB_ROWS / 128; ++c)
+                tc_cp_sf<NCTA>(sf_col + 4 + 4 * c, smem_desc_plain_rows16(sfb + 512 * c));
+            }
+            const uint32_t a0 = sbase + C::OFF_A + stage * C::A_BYTES;
+            const uint32_t b0 = sbase + C::OFF_B + stage * C::B_BYTES;
+#pragma unroll
+            for (int k = 0; k < C::MMAS_PER_STAGE; ++k) {
+              const uint64_t ad = smem_desc_sw128(a0 + k * C::MMA_K_BYTES);
+              const uint64_t bd = smem_desc_sw128(b0 + k * C::MMA_K_BYTES);
+              uint32_t id = idesc_plain;
+              if constexpr (C::kMX) id = idesc_mxf8(BN, C::TILE_M, kb % 4, kb % 4);
+              const uint32_t accum = C::kF32S ? (k > 0 ? 1u : 0u) : ((kb > 0 || k > 0) ? 1u : 0u);
+              tc_mma<NCTA, KIND>(d_tmem, ad, bd, id, sf_col, sf_col + 4, accum);
+            }
+            tc_commit_all<NCTA>(bar(C::BAR_EMPTY + stage));
+            if constexpr (C::kMX) {
+              if (kb % 4 == 3 || kb == nkb - 1) tc_commit<NCTA>(bar(C::BAR_SF_FREE + slot));
+            }
+            if constexpr (C::kF32S) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
+          }
+          __syncwarp();
+          if constexpr (C::kMX) {
+            if (kb % 4 == 3 || kb == nkb - 1) {
+              if (slot) ++sf_uses1; else ++sf_uses0;
+              ++gctr;
+            }
+          }
+          if constexpr (C::kF32S) {
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if constexpr (!C::kF32S) {
+          if (lane == 0) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
+          __syncwarp();
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+      }
+      aborted = !ok;
+      // every tcgen05 op issued completes before TMEM is released
+      if (lane == 0) tc_commit<NCTA>(bar(C::BAR_DRAIN));
+      __syncwarp();
+      PairWaitCtl drain = ctl;
+      uint32_t zero = 0;
+      drain.abort_flag = &zero;
+      drain.peer_abort = 0;
+      pwait(bar(C::BAR_DRAIN), 0u, drain);
+    }
+  } else if (C::kMX && warp == 2) {
+    // ============================================================ scale-word transposer
+    ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
+    int stage = 0;
+    uint32_t sfl_bits = 0;
+    bool ok = true;
+    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+      Tile tl;
+      if (!get_tile(t, tl)) continue;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (kb % 4 == 0) {
+          if (!pwait(bar(C::BAR_SFL + stage), (sfl_bits >> stage) & 1u, ctl)) { ok = false; break; }
+          sfl_bits ^= 1u << stage;
+          uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::OFF_SFA + stage * C::SFA_BYTES);
+          uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + C::OFF_SFB + stage * C::SFB_BYTES);
+          sf_transpose(sfa, lane);
+#pragma unroll
+          for (int c = 0; c < C::SFB_ROWS / 128; ++c) sf_transpose(sfb + 128 * c, lane);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + stage));
+        }
+        if (++stage == STAGES) stage = 0;
+      }
+    }
+    aborted = !ok;
+  } else if constexpr (!C::kF32S) {
+    // ============================================================ epilogue
+    ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
+    const uint32_t q = warp & 3u;
+    const bool bf16 = args.out_bf16 != 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      Tile tl;
+      if (!get_tile(t, tl)) continue;
+      if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const int r = static_cast<int>(q * 32 + lane);
+      bool row_ok = r < tl.row_limit;
+      if constexpr (SCHED == Sched::Contiguous) {
+        if (row_ok) {
+          const int g = __ldg(args.m_indices + tl.a_row0 + r);
+          if (g != tl.group) {
+            if (g >= 0) atomicOr(args.status, FGF8_DEVERR_INPUT);
+            row_ok = false;
+          }
+        }
+      }
+      const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
+      const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
+        ptx::tmem_wait_ld();
+        if (c == BN / 32 - 1) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
+        }
+        if (row_ok)
+          store_row32(args.D, row_off, tl.n_blk * BN + 32 * c, N, reinterpret_cast<const float*>(v), bf16);
+      }
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    aborted = !ok;
+  } else {
+    // ============================================================ promotion
+    ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
+    constexpr int HALF = BN / 2;
+    const uint32_t q = warp & 3u;
+    const int h = static_cast<int>(warp - C::EPI_WARP0) >> 2;
+    const bool bf16 = args.out_bf16 != 0;
+    const int nkb128 = K / 128;
+    const int nnb = (N + 127) / 128;
+    const int ld_a = (M + 3) / 4 * 4;
+    int pbuf = 0;
+    uint32_t pphase = 0;
+    bool ok = true;
+    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+      Tile tl;
+      if (!get_tile(t, tl)) continue;
+      const int r = static_cast<int>(q * 32 + lane);
+      bool row_ok = r < tl.row_limit;
+      if constexpr (SCHED == Sched::Contiguous) {
+        if (row_ok) {
+          const int g = __ldg(args.m_indices + tl.a_row0 + r);
+          if (g != tl.group) {
+            if (g >= 0) atomicOr(args.status, FGF8_DEVERR_INPUT);
+            row_ok = false;
+          }
+        }
+      }
+      const int col0 = tl.n_blk * BN + h * HALF;
+      const bool col_ok = col0 < N;
+      const float* sfa = args.sfa_f32 +
+                         (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * nkb128 * ld_a : 0) +
+                         (tl.m_blk + r);
+      const float* sfb = args.sfb_f32 +
+                         (static_cast<size_t>(tl.group) * nnb + (col_ok ? col0 / 128 : 0)) * nkb128;
+      float accv[HALF];
+#pragma unroll
+      for (int i = 0; i < HALF; ++i) accv[i] = 0.0f;
+      float sa = row_ok ? __ldg(sfa) : 0.0f;
+      float sb = col_ok ? __ldg(sfb) : 0.0f;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const float s = sa * sb;
+        if (kb + 1 < nkb) {
+          sa = row_ok ? __ldg(sfa + static_cast<size_t>(kb + 1) * ld_a) : 0.0f;
+          sb = col_ok ? __ldg(sfb + kb + 1) : 0.0f;
+        }
+        if (!pwait(bar(C::BAR_ACC_FULL + pbuf), pphase, ctl)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pbuf * BN + h * HALF);
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
+          ptx::tmem_wait_ld();
+          if (c == HALF / 32 - 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + pbuf));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) accv[32 * c + j] = fmaf(s, __uint_as_float(v[j]), accv[32 * c + j]);
+        }
+        if (++pbuf == 2) { pbuf = 0; pphase ^= 1u; }
+      }
+      if (!ok) break;
+      if (row_ok) {
+        const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) store_row32(args.D, row_off, col0 + 32 * c, N, accv + 32 * c, bf16);
+      }
+    }
+    aborted = !ok;
+  }
+
+  // ---------------------------------------------------------------- teardown
+  // After an abort, loads or MMAs may still be in flight toward this CTA's shared
+  // memory or TMEM: give them time to land (a few microseconds suffice) before the
+  // CTA may exit.  Normal completion never takes this path.
+  if (__syncthreads_or(aborted ? 1 : 0) || *abort_flag) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 200000ull) __nanosleep(1000);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if constexpr (NCTA == 2) cluster_sync_all();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    tc_dealloc<NCTA>(tmem_base, C::TMEM_ALLOC);
+  }
+}
+
+}  // namespace fgf8

@@ -117,3 +117,41 @@ def test_host_validation_errors(fg, dev):
     with pytest.raises(fg.FGF8Error) as e:
         fg.gemm_fp8_blockscaled(a, a, a, a, 0)
     assert e.value.code == 2
+
+
+# Every tile configuration the launchers can pick, forced through FGF8_FORCE_TILE
+# (one CTA per tile, or a CTA pair with M = 256 and B split across the pair).
+MXF8_TILES = ["2x224", "2x128", "1x224", "1x128", "1x64", "1x32"]
+F8F32_TILES = ["2x256", "1x256", "1x128", "1x64"]
+F16_TILES = ["2x256", "1x128"]
+
+
+@pytest.mark.parametrize("tile", MXF8_TILES)
+@pytest.mark.parametrize("M,N,K", [(384, 448, 640), (130, 96, 512)])
+def test_fp8_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    case = _fp8_case(M, N, K, 1, 300 + M)
+    out = _run_fp8(fg, dev, case, 1, M, N)
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 1), f"ue8m0 {tile} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("tile", F8F32_TILES)
+@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 512)])
+def test_fp8_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    case = _fp8_case(M, N, K, 0, 400 + M)
+    out = _run_fp8(fg, dev, case, 0, M, N)
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 0), f"f32 {tile} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("tile", F16_TILES)
+@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200)])
+def test_f16_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    a = inputs.uniform_16bit((M, K), 500 + M, dtype=torch.bfloat16)
+    b = inputs.uniform_16bit((N, K), 501 + N, dtype=torch.bfloat16)
+    out = fg.gemm_f16(a.to(dev), b.to(dev))
+    rc, _ = fg.check_status()
+    assert rc == 0
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_f16(a.float().numpy(), b.float().numpy()),
+               f"f16 {tile} {M}x{N}x{K}")

@@ -164,3 +164,33 @@ def test_masked_bad_count_is_reported(fg, dev):
     out = _run_masked(fg, dev, case, (5, 1000), 0)
     rc, bits = fg.check_status()
     assert rc == 6 and bits & 2
+
+
+@pytest.mark.parametrize("tile", ["2x224", "2x128", "1x224", "1x64"])
+def test_masked_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    masked = (0, 256, 17, 200)
+    case = _masked_case(4, 256, 448, 384, 1, 6)
+    out = _run_masked(fg, dev, case, masked, 1)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ref, valid = oracle.grouped_masked(*case, np.asarray(masked, np.int32), 1)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    gemm_close(o[v], ref[v], f"masked {tile}")
+    assert np.isnan(o[~v]).all()
+
+
+@pytest.mark.parametrize("tile", ["2x256", "1x256", "1x128"])
+def test_masked_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    masked = (0, 256, 17, 200)
+    case = _masked_case(4, 256, 512, 384, 0, 7)
+    out = _run_masked(fg, dev, case, masked, 0)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ref, valid = oracle.grouped_masked(*case, np.asarray(masked, np.int32), 0)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    gemm_close(o[v], ref[v], f"masked f32 {tile}")
+    assert np.isnan(o[~v]).all()
