@@ -9,12 +9,13 @@ template <Sched S>
 int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
                cudaStream_t stream) {
   if constexpr (S != Sched::Contiguous) {
-    if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 256, 6>(a, tm, tiles, stream);
+    // pairs: 128-wide tiles so that four partial buffers fit in TMEM
+    if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 9, 4>(a, tm, tiles, stream);
   }
   switch (c.bn) {
     case 256: return launch_persistent<Kind::F8F32, S, 1, 256, 4>(a, tm, tiles, stream);
-    case 128: return launch_persistent<Kind::F8F32, S, 1, 128, 6>(a, tm, tiles, stream);
-    default: return launch_persistent<Kind::F8F32, S, 1, 64, 8>(a, tm, tiles, stream);
+    case 128: return launch_persistent<Kind::F8F32, S, 1, 128, 6, 4>(a, tm, tiles, stream);
+    default: return launch_persistent<Kind::F8F32, S, 1, 64, 8, 4>(a, tm, tiles, stream);
   }
 }
 
@@ -22,7 +23,7 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
                       cudaStream_t stream) {
-  static const TileCfg pair_cands[] = {{2, 256}, {1, 256}, {1, 128}, {1, 64}};
+  static const TileCfg pair_cands[] = {{2, 128}, {1, 256}, {1, 128}, {1, 64}};
   static const TileCfg single_cands[] = {{1, 256}, {1, 128}, {1, 64}};
   const bool pairs = sched != Sched::Contiguous;
   const TileCfg* cands = pairs ? pair_cands : single_cands;

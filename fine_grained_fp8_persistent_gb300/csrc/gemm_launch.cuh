@@ -53,10 +53,14 @@ inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
   return best;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES>
+// Largest dynamic shared memory a CTA may opt into on sm_100-class parts (227 KB).
+constexpr int kMaxSmemOptin = 232448;
+
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2>
 int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES>;
-  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>;
+  static_assert(C::SMEM_BYTES <= kMaxSmemOptin, "shared memory budget");
+  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC>;
   static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

@@ -10,12 +10,13 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
                cudaStream_t stream) {
   if constexpr (S != Sched::Contiguous) {
     if (c.ncta == 2) {
-      if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 6>(a, tm, tiles, stream);
-      return launch_persistent<Kind::MXF8, S, 2, 128, 8>(a, tm, tiles, stream);
+      if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 7>(a, tm, tiles, stream);
+      return launch_persistent<Kind::MXF8, S, 2, 128, 9>(a, tm, tiles, stream);
     }
   }
   switch (c.bn) {
-    case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 4>(a, tm, tiles, stream);
+    // the masked scheduler's per-expert prefix takes the room of a fifth stage
+    case 224: return launch_persistent<Kind::MXF8, S, 1, 224, S == Sched::Masked ? 4 : 5>(a, tm, tiles, stream);
     case 128: return launch_persistent<Kind::MXF8, S, 1, 128, 6>(a, tm, tiles, stream);
     case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 8>(a, tm, tiles, stream);
     default: return launch_persistent<Kind::MXF8, S, 1, 32, 8>(a, tm, tiles, stream);

@@ -17,9 +17,11 @@
 //            stages.  In a pair both CTAs' loads complete on the even CTA's `full`
 //            barrier (cp.async.bulk.tensor .cta_group::2).
 //   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).
-//   warp 2   (UE8M0 kernels) scale-word transposer: after a stage's packed scale
-//            words land, rearranges them into the 32 x 128-bit layout tcgen05.cp
-//            copies and tells the MMA issuer (`sf_ready`, counted over the pair).
+//   warp 2   (UE8M0 kernels) scale-word producer: loads the packed scale words of
+//            each group of four K blocks into a small ring of its own, running
+//            ahead of the MMA, rearranges them into the 32 x 128-bit layout
+//            tcgen05.cp copies and tells the MMA issuer (`sf_ready`, counted
+//            over the pair), so scale traffic never sits on the MMA's path.
 //   rest     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
 //            promotion (8 warps: per-128-K partial from TMEM, acc += sA*sB*partial
 //            on the CUDA cores, the DeepGEMM page's promotion loop).
@@ -191,7 +193,7 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_>
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
   static constexpr int BM = 128;                    // rows per CTA
@@ -218,26 +220,31 @@ struct PCfg {
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr int MAX_GROUPS = 1024;
 
+  // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
+  // the per-K-block partials of the FP32-scale path (promotion latency slack).
+  static constexpr int NACC = NACC_;
+  static constexpr int SF_RING = 3;                 // scale-word groups in flight
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_BAR = (OFF_SFB + STAGES * SFB_BYTES + 7) / 8 * 8;
+  static constexpr int OFF_SFB = OFF_SFA + SF_RING * SFA_BYTES;
+  static constexpr int OFF_BAR = (OFF_SFB + SF_RING * SFB_BYTES + 7) / 8 * 8;
   static constexpr int BAR_FULL = 0;
   static constexpr int BAR_EMPTY = STAGES;
-  static constexpr int BAR_SFL = 2 * STAGES;        // scale words landed (local)
-  static constexpr int BAR_SFR = 3 * STAGES;        // scale words transposed (even CTA, pair count)
-  static constexpr int BAR_ACC_FULL = 4 * STAGES;   // 2
-  static constexpr int BAR_ACC_EMPTY = 4 * STAGES + 2;
-  static constexpr int BAR_SF_FREE = 4 * STAGES + 4;
-  static constexpr int BAR_DRAIN = 4 * STAGES + 6;
-  static constexpr int NUM_BARS = 4 * STAGES + 7;
+  static constexpr int BAR_ACC_FULL = 2 * STAGES;                 // NACC
+  static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + NACC;       // NACC
+  static constexpr int BAR_SFL = BAR_ACC_EMPTY + NACC;            // SF_RING: words landed (local)
+  static constexpr int BAR_SFR = BAR_SFL + SF_RING;               // SF_RING: transposed (even CTA)
+  static constexpr int BAR_SF_SMEM_FREE = BAR_SFR + SF_RING;      // SF_RING: copied to TMEM (local)
+  static constexpr int BAR_SF_FREE = BAR_SF_SMEM_FREE + SF_RING;  // 2 TMEM scale slots
+  static constexpr int BAR_DRAIN = BAR_SF_FREE + 2;
+  static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
   static constexpr int PREFIX_BYTES = (SCHED == Sched::Masked) ? (MAX_GROUPS + 1) * 4 : 0;
   static constexpr int SMEM_BYTES = OFF_PREFIX + PREFIX_BYTES + 1024;
 
-  static constexpr int ACC_COLS = 2 * BN;
+  static constexpr int ACC_COLS = NACC * BN;
   static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
   static constexpr int SF_COL0 = ACC_COLS;
   static constexpr int TMEM_USED = ACC_COLS + (kMX ? 2 * SF_SLOT_COLS : 0);
@@ -249,6 +256,7 @@ struct PCfg {
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
   static constexpr uint32_t SF_TX = BM * 4 + BN * 4;             // bytes landing on `sf_loaded`
+  static_assert(NACC >= 2 && (kF32S || NACC == 2), "accumulator buffers");
 };
 
 // Rearranges 128 packed scale words (row-major over 128 rows) in place so that
@@ -288,12 +296,12 @@ __device__ __forceinline__ void store_row32(void* D, size_t row_off, int col0, i
   }
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES>
-__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 1)
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -323,14 +331,17 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar(C::BAR_FULL + s), 1);
       ptx::mbar_init(bar(C::BAR_EMPTY + s), 1);
-      ptx::mbar_init(bar(C::BAR_SFL + s), 1);
-      ptx::mbar_init(bar(C::BAR_SFR + s), NCTA);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
       ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
-      ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
     }
+    for (int r = 0; r < C::SF_RING; ++r) {
+      ptx::mbar_init(bar(C::BAR_SFL + r), 1);
+      ptx::mbar_init(bar(C::BAR_SFR + r), NCTA);
+      ptx::mbar_init(bar(C::BAR_SF_SMEM_FREE + r), 1);
+    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
     ptx::mbar_init(bar(C::BAR_DRAIN), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -414,10 +425,6 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_a);
       ptx::prefetch_tmap(&tm_b);
-      if constexpr (C::kMX) {
-        ptx::prefetch_tmap(&tm_sfa);
-        ptx::prefetch_tmap(&tm_sfb);
-      }
     }
     int stage = 0;
     uint32_t phase = 0;
@@ -432,14 +439,6 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
           if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
           tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
           tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
-          if (C::kMX && kb % 4 == 0) {
-            const uint32_t sfl = bar(C::BAR_SFL + stage);
-            ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
-            const int sfa_row = (SCHED == Sched::Masked ? tl.group * kq : 0) + kb / 4;
-            ptx::tma_load_2d(sbase + C::OFF_SFA + stage * C::SFA_BYTES, &tm_sfa, sfl, tl.m_blk, sfa_row);
-            ptx::tma_load_2d(sbase + C::OFF_SFB + stage * C::SFB_BYTES, &tm_sfb, sfl, tl.n_blk * BN,
-                             tl.group * kq + kb / 4);
-          }
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -451,10 +450,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
     ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
     if (leader) {
       int stage = 0;
-      uint32_t phase = 0, sfr_bits = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t sf_uses0 = 0u, sf_uses1 = 0u, gctr = 0u;
+      uint32_t gctr = 0u;            // scale-word groups consumed so far (all tiles)
       bool ok = true;
       const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
       const uint32_t idesc_plain = idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
@@ -464,7 +463,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
         if constexpr (!C::kF32S) {
           if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
         }
-        uint32_t slot = 0;
+        uint32_t slot = 0, ring = 0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!pwait(bar(C::BAR_FULL + stage), phase, ctl)) { ok = false; break; }
           if constexpr (C::kF32S) {
@@ -472,19 +471,19 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
           }
           const bool sf_block = C::kMX && (kb % 4 == 0);
           if (sf_block) {
+            // TMEM scale slot gctr % 2 was last read by group gctr - 2
             slot = gctr & 1u;
-            const uint32_t uses = slot ? sf_uses1 : sf_uses0;
-            if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
-            if (!pwait(bar(C::BAR_SFR + stage), (sfr_bits >> stage) & 1u, ctl)) { ok = false; break; }
-            sfr_bits ^= 1u << stage;
+            if (gctr >= 2 && !pwait(bar(C::BAR_SF_FREE + slot), ((gctr >> 1) - 1u) & 1u, ctl)) { ok = false; break; }
+            ring = gctr % C::SF_RING;
+            if (!pwait(bar(C::BAR_SFR + ring), (gctr / C::SF_RING) & 1u, ctl)) { ok = false; break; }
           }
           ptx::tc_fence_after();
           if (lane == 0) {
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
             if (sf_block) {
-              const uint32_t sfa = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
-              const uint32_t sfb = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+              const uint32_t sfa = sbase + C::OFF_SFA + ring * C::SFA_BYTES;
+              const uint32_t sfb = sbase + C::OFF_SFB + ring * C::SFB_BYTES;
               tc_cp_sf<NCTA>(sf_col, smem_desc_plain_rows16(sfa));
 #pragma unroll
               for (int c = 0; c < C::SFB_ROWS / 128; ++c)
@@ -503,19 +502,19 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
             }
             tc_commit_all<NCTA>(bar(C::BAR_EMPTY + stage));
             if constexpr (C::kMX) {
-              if (kb % 4 == 3 || kb == nkb - 1) tc_commit<NCTA>(bar(C::BAR_SF_FREE + slot));
+              if (kb % 4 == 3 || kb == nkb - 1) {
+                tc_commit<NCTA>(bar(C::BAR_SF_FREE + slot));
+                tc_commit_all<NCTA>(bar(C::BAR_SF_SMEM_FREE + ring));
+              }
             }
             if constexpr (C::kF32S) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
           }
           __syncwarp();
           if constexpr (C::kMX) {
-            if (kb % 4 == 3 || kb == nkb - 1) {
-              if (slot) ++sf_uses1; else ++sf_uses0;
-              ++gctr;
-            }
+            if (kb % 4 == 3 || kb == nkb - 1) ++gctr;
           }
           if constexpr (C::kF32S) {
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -523,7 +522,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
         if constexpr (!C::kF32S) {
           if (lane == 0) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
           __syncwarp();
-          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+          if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
         }
       }
       aborted = !ok;
@@ -537,28 +536,40 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
       pwait(bar(C::BAR_DRAIN), 0u, drain);
     }
   } else if (C::kMX && warp == 2) {
-    // ============================================================ scale-word transposer
-    ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
-    int stage = 0;
-    uint32_t sfl_bits = 0;
+    // ============================================================ scale-word producer
+    ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_sfa);
+      ptx::prefetch_tmap(&tm_sfb);
+    }
+    uint32_t gctr = 0;
     bool ok = true;
     for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
       Tile tl;
       if (!get_tile(t, tl)) continue;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (kb % 4 == 0) {
-          if (!pwait(bar(C::BAR_SFL + stage), (sfl_bits >> stage) & 1u, ctl)) { ok = false; break; }
-          sfl_bits ^= 1u << stage;
-          uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::OFF_SFA + stage * C::SFA_BYTES);
-          uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + C::OFF_SFB + stage * C::SFB_BYTES);
-          sf_transpose(sfa, lane);
-#pragma unroll
-          for (int c = 0; c < C::SFB_ROWS / 128; ++c) sf_transpose(sfb + 128 * c, lane);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + stage));
+      for (int kb = 0; kb < nkb; kb += 4, ++gctr) {
+        const uint32_t ring = gctr % C::SF_RING;
+        const uint32_t round = gctr / C::SF_RING;
+        // the ring slot is free once the group that used it was copied to TMEM
+        if (!pwait(bar(C::BAR_SF_SMEM_FREE + ring), (round & 1u) ^ 1u, ctl)) { ok = false; break; }
+        const uint32_t sfl = bar(C::BAR_SFL + ring);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
+          const int sfa_row = (SCHED == Sched::Masked ? tl.group * kq : 0) + kb / 4;
+          ptx::tma_load_2d(sbase + C::OFF_SFA + ring * C::SFA_BYTES, &tm_sfa, sfl, tl.m_blk, sfa_row);
+          ptx::tma_load_2d(sbase + C::OFF_SFB + ring * C::SFB_BYTES, &tm_sfb, sfl, tl.n_blk * BN,
+                           tl.group * kq + kb / 4);
         }
-        if (++stage == STAGES) stage = 0;
+        __syncwarp();
+        if (!pwait(sfl, round & 1u, ctl)) { ok = false; break; }
+        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::OFF_SFA + ring * C::SFA_BYTES);
+        uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + C::OFF_SFB + ring * C::SFB_BYTES);
+        sf_transpose(sfa, lane);
+#pragma unroll
+        for (int c = 0; c < C::SFB_ROWS / 128; ++c) sf_transpose(sfb + 128 * c, lane);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + ring));
       }
     }
     aborted = !ok;
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
         if (row_ok)
           store_row32(args.D, row_off, tl.n_blk * BN + 32 * c, N, reinterpret_cast<const float*>(v), bf16);
       }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }
     aborted = !ok;
   } else {
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES>::THREADS, 
 #pragma unroll
           for (int j = 0; j < 32; ++j) accv[32 * c + j] = fmaf(s, __uint_as_float(v[j]), accv[32 * c + j]);
         }
-        if (++pbuf == 2) { pbuf = 0; pphase ^= 1u; }
+        if (++pbuf == C::NACC) { pbuf = 0; pphase ^= 1u; }
       }
       if (!ok) break;
       if (row_ok) {

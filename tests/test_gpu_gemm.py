@@ -122,7 +122,7 @@ def test_host_validation_errors(fg, dev):
 # Every tile configuration the launchers can pick, forced through FGF8_FORCE_TILE
 # (one CTA per tile, or a CTA pair with M = 256 and B split across the pair).
 MXF8_TILES = ["2x224", "2x128", "1x224", "1x128", "1x64", "1x32"]
-F8F32_TILES = ["2x256", "1x256", "1x128", "1x64"]
+F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
 F16_TILES = ["2x256", "1x128"]
 
 
