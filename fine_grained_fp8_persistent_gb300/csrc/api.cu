@@ -264,8 +264,11 @@ static int check_fp8_common(const char* who, int N, int K, int fmt) {
 
 static int dispatch_fp8(fgf8::GemmArgs& a, fgf8::Sched sched, const void* Aq, const void* SFA,
                         const void* Bq, const void* SFB, int fmt, void* stream) {
-  if (fmt == FGF8_SCALE_UE8M0)
+  if (fmt == FGF8_SCALE_UE8M0) {
+    a.sfa_ue8m0 = static_cast<const uint32_t*>(SFA);
+    a.sfb_ue8m0 = static_cast<const uint32_t*>(SFB);
     return fgf8::launch_gemm_mxf8(a, sched, Aq, SFA, Bq, SFB, static_cast<cudaStream_t>(stream));
+  }
   a.sfa_f32 = static_cast<const float*>(SFA);
   a.sfb_f32 = static_cast<const float*>(SFB);
   return fgf8::launch_gemm_f8f32(a, sched, Aq, Bq, static_cast<cudaStream_t>(stream));

@@ -32,6 +32,8 @@ struct GemmArgs {
   int out_bf16;               // 1: bf16 output, 0: fp16 output
   const float* sfa_f32;       // FP32-scale path: activation scales
   const float* sfb_f32;       // FP32-scale path: weight block scales
+  const uint32_t* sfa_ue8m0;  // UE8M0 path: packed activation scale words
+  const uint32_t* sfb_ue8m0;  // UE8M0 path: packed weight scale words
   uint32_t* status;           // device status word
   uint64_t timeout_ns;        // bound on every barrier wait
 };

@@ -17,11 +17,16 @@
 //            stages.  In a pair both CTAs' loads complete on the even CTA's `full`
 //            barrier (cp.async.bulk.tensor .cta_group::2).
 //   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).
-//   warp 2   (UE8M0 kernels) scale-word producer: loads the packed scale words of
-//            each group of four K blocks into a small ring of its own, running
-//            ahead of the MMA, rearranges them into the 32 x 128-bit layout
-//            tcgen05.cp copies and tells the MMA issuer (`sf_ready`, counted
-//            over the pair), so scale traffic never sits on the MMA's path.
+//   warps 2-5 (UE8M0 kernels) scale-factor writers, one per TMEM lane quarter:
+//            for each group of four K blocks they read the packed scale words
+//            from global memory and write them into a double-buffered TMEM slot
+//            with tcgen05.st (each quarter gets the same copy), then signal the
+//            MMA issuer (`sf_ready`, counted over the pair).  The block-scaled MMA
+//            reads A's scale of row 32 j + l and B's scale of row 32 j + l from
+//            lane l, column j of its slot ("Blackwell Tensor Core: tcgen05.mma",
+//            Block-Scaled MMA: SFA/SFB live in TMEM).  Writing them from the
+//            warps keeps the copy out of the tensor pipe: a tcgen05.cp issued
+//            between MMAs stalls the MMA stream for several hundred cycles.
 //   rest     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
 //            promotion (8 warps: per-128-K partial from TMEM, acc += sA*sB*partial
 //            on the CUDA cores, the DeepGEMM page's promotion loop).
@@ -114,14 +119,6 @@ __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
   else
     ptx::tmem_dealloc(taddr, ncols);
 }
-template <int NCTA>
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  if constexpr (NCTA == 2)
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-  else
-    ptx::tmem_cp_32x128b_warpx4(taddr, sdesc);
-}
 template <int NCTA, Kind KIND>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t acc) {
@@ -150,6 +147,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uin
     else if constexpr (KIND == Kind::F8F32) ptx::mma_f8(d, ad, bd, idesc, acc);
     else ptx::mma_f16(d, ad, bd, idesc, acc);
   }
+}
+
+// 32 lanes x 4 columns of 32 bits from registers into TMEM (thread l -> lane base + l).
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Bounded wait with cluster-scope acquire (barriers that receive the peer's arrivals).
@@ -212,9 +219,7 @@ struct PCfg {
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
-  static constexpr int SFA_BYTES = kMX ? BM * 4 : 0;
-  static constexpr int SFB_BYTES = kMX ? SFB_ROWS * 4 : 0;
-  static constexpr int SF_WARPS = kMX ? 1 : 0;
+  static constexpr int SF_WARPS = kMX ? 4 : 0;
   static constexpr int EPI_WARPS = kF32S ? 8 : 4;
   static constexpr int EPI_WARP0 = 2 + SF_WARPS;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -223,20 +228,15 @@ struct PCfg {
   // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
   // the per-K-block partials of the FP32-scale path (promotion latency slack).
   static constexpr int NACC = NACC_;
-  static constexpr int SF_RING = 3;                 // scale-word groups in flight
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + SF_RING * SFA_BYTES;
-  static constexpr int OFF_BAR = (OFF_SFB + SF_RING * SFB_BYTES + 7) / 8 * 8;
+  static constexpr int OFF_BAR = (OFF_B + STAGES * B_BYTES + 7) / 8 * 8;
   static constexpr int BAR_FULL = 0;
   static constexpr int BAR_EMPTY = STAGES;
   static constexpr int BAR_ACC_FULL = 2 * STAGES;                 // NACC
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + NACC;       // NACC
-  static constexpr int BAR_SFL = BAR_ACC_EMPTY + NACC;            // SF_RING: words landed (local)
-  static constexpr int BAR_SFR = BAR_SFL + SF_RING;               // SF_RING: transposed (even CTA)
-  static constexpr int BAR_SF_SMEM_FREE = BAR_SFR + SF_RING;      // SF_RING: copied to TMEM (local)
-  static constexpr int BAR_SF_FREE = BAR_SF_SMEM_FREE + SF_RING;  // 2 TMEM scale slots
+  static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // 2: scale slot written (even CTA)
+  static constexpr int BAR_SF_FREE = BAR_SFR + 2;                 // 2: scale slot read (each CTA)
   static constexpr int BAR_DRAIN = BAR_SF_FREE + 2;
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -255,18 +255,8 @@ struct PCfg {
                                                        : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
-  static constexpr uint32_t SF_TX = BM * 4 + BN * 4;             // bytes landing on `sf_loaded`
   static_assert(NACC >= 2 && (kF32S || NACC == 2), "accumulator buffers");
 };
-
-// Rearranges 128 packed scale words (row-major over 128 rows) in place so that
-// row 32 j + l sits at word 4 l + j: TMEM lane l, column j after tcgen05.cp.
-__device__ __forceinline__ void sf_transpose(uint32_t* p, uint32_t lane) {
-  const uint32_t v0 = p[lane], v1 = p[32 + lane], v2 = p[64 + lane], v3 = p[96 + lane];
-  __syncwarp();
-  *reinterpret_cast<uint4*>(p + 4 * lane) = make_uint4(v0, v1, v2, v3);
-  __syncwarp();
-}
 
 __device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
   if (bf16) {
@@ -336,12 +326,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
       ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
     }
-    for (int r = 0; r < C::SF_RING; ++r) {
-      ptx::mbar_init(bar(C::BAR_SFL + r), 1);
-      ptx::mbar_init(bar(C::BAR_SFR + r), NCTA);
-      ptx::mbar_init(bar(C::BAR_SF_SMEM_FREE + r), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
+      ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
     }
-    for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
     ptx::mbar_init(bar(C::BAR_DRAIN), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -463,32 +451,21 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
         if constexpr (!C::kF32S) {
           if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
         }
-        uint32_t slot = 0, ring = 0;
+        uint32_t slot = 0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!pwait(bar(C::BAR_FULL + stage), phase, ctl)) { ok = false; break; }
           if constexpr (C::kF32S) {
             if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
           }
-          const bool sf_block = C::kMX && (kb % 4 == 0);
-          if (sf_block) {
-            // TMEM scale slot gctr % 2 was last read by group gctr - 2
+          if (C::kMX && kb % 4 == 0) {
+            // the scale writers filled slot gctr % 2 for this group of four K blocks
             slot = gctr & 1u;
-            if (gctr >= 2 && !pwait(bar(C::BAR_SF_FREE + slot), ((gctr >> 1) - 1u) & 1u, ctl)) { ok = false; break; }
-            ring = gctr % C::SF_RING;
-            if (!pwait(bar(C::BAR_SFR + ring), (gctr / C::SF_RING) & 1u, ctl)) { ok = false; break; }
+            if (!pwait(bar(C::BAR_SFR + slot), (gctr >> 1) & 1u, ctl)) { ok = false; break; }
           }
           ptx::tc_fence_after();
           if (lane == 0) {
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-            if (sf_block) {
-              const uint32_t sfa = sbase + C::OFF_SFA + ring * C::SFA_BYTES;
-              const uint32_t sfb = sbase + C::OFF_SFB + ring * C::SFB_BYTES;
-              tc_cp_sf<NCTA>(sf_col, smem_desc_plain_rows16(sfa));
-#pragma unroll
-              for (int c = 0; c < C::SFB_ROWS / 128; ++c)
-                tc_cp_sf<NCTA>(sf_col + 4 + 4 * c, smem_desc_plain_rows16(sfb + 512 * c));
-            }
             const uint32_t a0 = sbase + C::OFF_A + stage * C::A_BYTES;
             const uint32_t b0 = sbase + C::OFF_B + stage * C::B_BYTES;
 #pragma unroll
@@ -502,10 +479,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
             }
             tc_commit_all<NCTA>(bar(C::BAR_EMPTY + stage));
             if constexpr (C::kMX) {
-              if (kb % 4 == 3 || kb == nkb - 1) {
-                tc_commit<NCTA>(bar(C::BAR_SF_FREE + slot));
-                tc_commit_all<NCTA>(bar(C::BAR_SF_SMEM_FREE + ring));
-              }
+              if (kb % 4 == 3 || kb == nkb - 1) tc_commit_all<NCTA>(bar(C::BAR_SF_FREE + slot));
             }
             if constexpr (C::kF32S) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
           }
@@ -535,41 +509,49 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       drain.peer_abort = 0;
       pwait(bar(C::BAR_DRAIN), 0u, drain);
     }
-  } else if (C::kMX && warp == 2) {
-    // ============================================================ scale-word producer
+  } else if (C::kMX && warp < 2 + C::SF_WARPS) {
+    // ============================================================ scale-factor writers
     ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tm_sfa);
-      ptx::prefetch_tmap(&tm_sfb);
-    }
+    const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp writes
+    const int ld_a = (M + 3) / 4 * 4;                  // rows of one activation table
+    const int ld_n = (N + 3) / 4 * 4;
+    constexpr int NB_COLS = C::SFB_ROWS / 32;
     uint32_t gctr = 0;
     bool ok = true;
     for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
       Tile tl;
       if (!get_tile(t, tl)) continue;
+      const uint32_t* sfa_tab = args.sfa_ue8m0 +
+                                (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * kq * ld_a : 0);
+      const uint32_t* sfb_tab = args.sfb_ue8m0 + static_cast<size_t>(tl.group) * kq * ld_n;
+      const int n0 = tl.n_blk * BN;
       for (int kb = 0; kb < nkb; kb += 4, ++gctr) {
-        const uint32_t ring = gctr % C::SF_RING;
-        const uint32_t round = gctr / C::SF_RING;
-        // the ring slot is free once the group that used it was copied to TMEM
-        if (!pwait(bar(C::BAR_SF_SMEM_FREE + ring), (round & 1u) ^ 1u, ctl)) { ok = false; break; }
-        const uint32_t sfl = bar(C::BAR_SFL + ring);
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
-          const int sfa_row = (SCHED == Sched::Masked ? tl.group * kq : 0) + kb / 4;
-          ptx::tma_load_2d(sbase + C::OFF_SFA + ring * C::SFA_BYTES, &tm_sfa, sfl, tl.m_blk, sfa_row);
-          ptx::tma_load_2d(sbase + C::OFF_SFB + ring * C::SFB_BYTES, &tm_sfb, sfl, tl.n_blk * BN,
-                           tl.group * kq + kb / 4);
-        }
-        __syncwarp();
-        if (!pwait(sfl, round & 1u, ctl)) { ok = false; break; }
-        uint32_t* sfa = reinterpret_cast<uint32_t*>(smem + C::OFF_SFA + ring * C::SFA_BYTES);
-        uint32_t* sfb = reinterpret_cast<uint32_t*>(smem + C::OFF_SFB + ring * C::SFB_BYTES);
-        sf_transpose(sfa, lane);
+        // column j of lane l holds the word of row 32 j + l (of this CTA's A rows,
+        // of the tile's B rows); rows outside the tables read as 0
+        const size_t qrow = static_cast<size_t>(kb / 4);
+        uint32_t a[4], b[NB_COLS];
 #pragma unroll
-        for (int c = 0; c < C::SFB_ROWS / 128; ++c) sf_transpose(sfb + 128 * c, lane);
-        ptx::fence_proxy_async_smem();
+        for (int j = 0; j < 4; ++j) {
+          const int m = tl.m_blk + 32 * j + static_cast<int>(lane);
+          a[j] = (m < ld_a) ? __ldg(sfa_tab + qrow * ld_a + m) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < NB_COLS; ++j) {
+          const int r = 32 * j + static_cast<int>(lane);
+          b[j] = (r < BN && n0 + r < ld_n) ? __ldg(sfb_tab + qrow * ld_n + n0 + r) : 0u;
+        }
+        const uint32_t slot = gctr & 1u;
+        // the slot was last read by group gctr - 2
+        if (gctr >= 2 && !pwait(bar(C::BAR_SF_FREE + slot), ((gctr >> 1) - 1u) & 1u, ctl)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+        tmem_st_x4(taddr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int j = 0; j < NB_COLS; j += 4) tmem_st_x4(taddr + 4 + j, b[j], b[j + 1], b[j + 2], b[j + 3]);
+        tmem_wait_st();
+        ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + ring));
+        if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + slot));
       }
     }
     aborted = !ok;
