@@ -49,13 +49,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode < 0 or "Segmentation fault" in r.stderr:
+            # a crashed compiler process (not a compile error) is retried once
+            r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
         if verbose:
             print(r.stdout + r.stderr)
 
     if jobs:
-        with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), 4, os.cpu_count() or 4))) as ex:
             list(ex.map(run, jobs))
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + ".tmp"

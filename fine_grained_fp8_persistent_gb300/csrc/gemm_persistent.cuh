@@ -326,9 +326,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
       ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
-      ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
+    if constexpr (C::kMX) {
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
+        ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
+      }
     }
     ptx::mbar_init(bar(C::BAR_DRAIN), 1);
     *abort_flag = 0u;
@@ -509,8 +511,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       drain.peer_abort = 0;
       pwait(bar(C::BAR_DRAIN), 0u, drain);
     }
-  } else if (C::kMX && warp < 2 + C::SF_WARPS) {
+  } else if (warp < 2 + C::SF_WARPS) {
     // ============================================================ scale-factor writers
+    if constexpr (C::kMX) {
     ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
     const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp writes
     const int ld_a = (M + 3) / 4 * 4;                  // rows of one activation table
@@ -555,6 +558,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       }
     }
     aborted = !ok;
+    }
   } else if constexpr (!C::kF32S) {
     // ============================================================ epilogue
     ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
