@@ -149,6 +149,14 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uin
   }
 }
 
+// Bring one tile of a tensor into L2 without writing shared memory.
+__device__ __forceinline__ void l2_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 32 lanes x 4 columns of 32 bits from registers into TMEM (thread l -> lane base + l).
 __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
@@ -235,9 +243,13 @@ struct PCfg {
   static constexpr int BAR_EMPTY = STAGES;
   static constexpr int BAR_ACC_FULL = 2 * STAGES;                 // NACC
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + NACC;       // NACC
-  static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // 2: scale slot written (even CTA)
-  static constexpr int BAR_SF_FREE = BAR_SFR + 2;                 // 2: scale slot read (each CTA)
-  static constexpr int BAR_DRAIN = BAR_SF_FREE + 2;
+  // TMEM scale slots: three where they fit next to the accumulators, so the
+  // scale writers can run two groups of K blocks ahead of the MMA
+  static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
+  static constexpr int SF_SLOTS = (2 * BN + 3 * SF_SLOT_COLS <= 512) ? 3 : 2;
+  static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // SF_SLOTS: slot written (even CTA)
+  static constexpr int BAR_SF_FREE = BAR_SFR + SF_SLOTS;          // SF_SLOTS: slot read (each CTA)
+  static constexpr int BAR_DRAIN = BAR_SF_FREE + SF_SLOTS;
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
@@ -245,9 +257,8 @@ struct PCfg {
   static constexpr int SMEM_BYTES = OFF_PREFIX + PREFIX_BYTES + 1024;
 
   static constexpr int ACC_COLS = NACC * BN;
-  static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
   static constexpr int SF_COL0 = ACC_COLS;
-  static constexpr int TMEM_USED = ACC_COLS + (kMX ? 2 * SF_SLOT_COLS : 0);
+  static constexpr int TMEM_USED = ACC_COLS + (kMX ? SF_SLOTS * SF_SLOT_COLS : 0);
   static constexpr int TMEM_ALLOC = TMEM_USED <= 32    ? 32
                                     : TMEM_USED <= 64  ? 64
                                     : TMEM_USED <= 128 ? 128
@@ -327,7 +338,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
     }
     if constexpr (C::kMX) {
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < C::SF_SLOTS; ++b) {
         ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
         ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
       }
@@ -429,6 +440,12 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
           if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
           tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
           tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
+          // pull the tiles of a later K block into L2 so that its load hits there
+          const int kp = kb + STAGES;
+          if (kp < nkb) {
+            l2_prefetch_2d(&tm_a, kp * C::BK, tl.a_row0);
+            l2_prefetch_2d(&tm_b, kp * C::BK, tl.b_row0);
+          }
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -460,9 +477,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
             if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
           }
           if (C::kMX && kb % 4 == 0) {
-            // the scale writers filled slot gctr % 2 for this group of four K blocks
-            slot = gctr & 1u;
-            if (!pwait(bar(C::BAR_SFR + slot), (gctr >> 1) & 1u, ctl)) { ok = false; break; }
+            // the scale writers filled this group's slot
+            slot = gctr % C::SF_SLOTS;
+            if (!pwait(bar(C::BAR_SFR + slot), (gctr / C::SF_SLOTS) & 1u, ctl)) { ok = false; break; }
           }
           ptx::tc_fence_after();
           if (lane == 0) {
@@ -519,43 +536,67 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
     const int ld_a = (M + 3) / 4 * 4;                  // rows of one activation table
     const int ld_n = (N + 3) / 4 * 4;
     constexpr int NB_COLS = C::SFB_ROWS / 32;
+    // Column j of lane l holds the word of row 32 j + l (of this CTA's A rows, of
+    // the tile's B rows); rows outside the tables read as 0.
+    auto load_words = [&](const Tile& tl, int kb, uint32_t (&a)[4], uint32_t (&b)[NB_COLS]) {
+      const uint32_t* sfa_tab = args.sfa_ue8m0 +
+                                (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * kq * ld_a : 0) +
+                                static_cast<size_t>(kb / 4) * ld_a;
+      const uint32_t* sfb_tab = args.sfb_ue8m0 + (static_cast<size_t>(tl.group) * kq + kb / 4) * ld_n;
+      const int n0 = tl.n_blk * BN;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int m = tl.m_blk + 32 * j + static_cast<int>(lane);
+        a[j] = (m < ld_a) ? __ldg(sfa_tab + m) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < NB_COLS; ++j) {
+        const int r = 32 * j + static_cast<int>(lane);
+        b[j] = (r < BN && n0 + r < ld_n) ? __ldg(sfb_tab + n0 + r) : 0u;
+      }
+    };
+    // walk (tile, group) in order, one group of loads in flight ahead of the writes
+    auto next_valid = [&](int t, Tile& tl) -> int {
+      for (; t < num_tiles; t += num_clusters)
+        if (get_tile(t, tl)) return t;
+      return num_tiles;
+    };
+    Tile tl_cur, tl_nxt;
+    int t_cur = next_valid(cluster_id, tl_cur), kb_cur = 0;
+    uint32_t a_cur[4], b_cur[NB_COLS], a_nxt[4], b_nxt[NB_COLS];
+    if (t_cur < num_tiles) load_words(tl_cur, 0, a_cur, b_cur);
     uint32_t gctr = 0;
     bool ok = true;
-    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
-      Tile tl;
-      if (!get_tile(t, tl)) continue;
-      const uint32_t* sfa_tab = args.sfa_ue8m0 +
-                                (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * kq * ld_a : 0);
-      const uint32_t* sfb_tab = args.sfb_ue8m0 + static_cast<size_t>(tl.group) * kq * ld_n;
-      const int n0 = tl.n_blk * BN;
-      for (int kb = 0; kb < nkb; kb += 4, ++gctr) {
-        // column j of lane l holds the word of row 32 j + l (of this CTA's A rows,
-        // of the tile's B rows); rows outside the tables read as 0
-        const size_t qrow = static_cast<size_t>(kb / 4);
-        uint32_t a[4], b[NB_COLS];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int m = tl.m_blk + 32 * j + static_cast<int>(lane);
-          a[j] = (m < ld_a) ? __ldg(sfa_tab + qrow * ld_a + m) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < NB_COLS; ++j) {
-          const int r = 32 * j + static_cast<int>(lane);
-          b[j] = (r < BN && n0 + r < ld_n) ? __ldg(sfb_tab + qrow * ld_n + n0 + r) : 0u;
-        }
-        const uint32_t slot = gctr & 1u;
-        // the slot was last read by group gctr - 2
-        if (gctr >= 2 && !pwait(bar(C::BAR_SF_FREE + slot), ((gctr >> 1) - 1u) & 1u, ctl)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-        tmem_st_x4(taddr, a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int j = 0; j < NB_COLS; j += 4) tmem_st_x4(taddr + 4 + j, b[j], b[j + 1], b[j + 2], b[j + 3]);
-        tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + slot));
+    while (ok && t_cur < num_tiles) {
+      int t_nxt = t_cur, kb_nxt = kb_cur + 4;
+      tl_nxt = tl_cur;
+      if (kb_nxt >= nkb) {
+        kb_nxt = 0;
+        t_nxt = next_valid(t_cur + num_clusters, tl_nxt);
       }
+      if (t_nxt < num_tiles) load_words(tl_nxt, kb_nxt, a_nxt, b_nxt);
+      const uint32_t slot = gctr % C::SF_SLOTS;
+      const uint32_t uses = gctr / C::SF_SLOTS;
+      // the slot was last read by group gctr - SF_SLOTS
+      if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
+      tmem_st_x4(taddr, a_cur[0], a_cur[1], a_cur[2], a_cur[3]);
+#pragma unroll
+      for (int j = 0; j < NB_COLS; j += 4)
+        tmem_st_x4(taddr + 4 + j, b_cur[j], b_cur[j + 1], b_cur[j + 2], b_cur[j + 3]);
+      tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + slot));
+      ++gctr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a_cur[j] = a_nxt[j];
+#pragma unroll
+      for (int j = 0; j < NB_COLS; ++j) b_cur[j] = b_nxt[j];
+      t_cur = t_nxt;
+      kb_cur = kb_nxt;
+      tl_cur = tl_nxt;
     }
     aborted = !ok;
     }
