@@ -149,14 +149,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uin
   }
 }
 
-// Bring one tile of a tensor into L2 without writing shared memory.
-__device__ __forceinline__ void l2_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // 32 lanes x 4 columns of 32 bits from registers into TMEM (thread l -> lane base + l).
 __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
@@ -440,12 +432,6 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
           if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
           tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
           tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
-          // pull the tiles of a later K block into L2 so that its load hits there
-          const int kp = kb + STAGES;
-          if (kp < nkb) {
-            l2_prefetch_2d(&tm_a, kp * C::BK, tl.a_row0);
-            l2_prefetch_2d(&tm_b, kp * C::BK, tl.b_row0);
-          }
         }
         __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -555,48 +541,58 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
         b[j] = (r < BN && n0 + r < ld_n) ? __ldg(sfb_tab + n0 + r) : 0u;
       }
     };
-    // walk (tile, group) in order, one group of loads in flight ahead of the writes
+    // Walk (tile, group) in order with two register sets: while group g is
+    // written from one set, the words of group g + 1 are already in flight into
+    // the other (the loop is unrolled by two so that no register copy waits on
+    // an outstanding load).
     auto next_valid = [&](int t, Tile& tl) -> int {
       for (; t < num_tiles; t += num_clusters)
         if (get_tile(t, tl)) return t;
       return num_tiles;
     };
-    Tile tl_cur, tl_nxt;
-    int t_cur = next_valid(cluster_id, tl_cur), kb_cur = 0;
-    uint32_t a_cur[4], b_cur[NB_COLS], a_nxt[4], b_nxt[NB_COLS];
-    if (t_cur < num_tiles) load_words(tl_cur, 0, a_cur, b_cur);
+    struct Pos { int t, kb; Tile tl; };
+    auto advance = [&](Pos& p) {
+      p.kb += 4;
+      if (p.kb >= nkb) {
+        p.kb = 0;
+        p.t = next_valid(p.t + num_clusters, p.tl);
+      }
+    };
+    Pos p0, p1;
+    p0.kb = 0;
+    p0.t = next_valid(cluster_id, p0.tl);
+    p1 = p0;
+    advance(p1);
+    uint32_t a0[4], b0[NB_COLS], a1[4], b1[NB_COLS];
+    if (p0.t < num_tiles) load_words(p0.tl, p0.kb, a0, b0);
+    if (p1.t < num_tiles) load_words(p1.tl, p1.kb, a1, b1);
     uint32_t gctr = 0;
     bool ok = true;
-    while (ok && t_cur < num_tiles) {
-      int t_nxt = t_cur, kb_nxt = kb_cur + 4;
-      tl_nxt = tl_cur;
-      if (kb_nxt >= nkb) {
-        kb_nxt = 0;
-        t_nxt = next_valid(t_cur + num_clusters, tl_nxt);
-      }
-      if (t_nxt < num_tiles) load_words(tl_nxt, kb_nxt, a_nxt, b_nxt);
+    // write one group from (a, b), then refill (a, b) with the group two ahead
+    auto write_group = [&](Pos& p, uint32_t (&a)[4], uint32_t (&b)[NB_COLS]) -> bool {
       const uint32_t slot = gctr % C::SF_SLOTS;
       const uint32_t uses = gctr / C::SF_SLOTS;
       // the slot was last read by group gctr - SF_SLOTS
-      if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
+      if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) return false;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-      tmem_st_x4(taddr, a_cur[0], a_cur[1], a_cur[2], a_cur[3]);
+      tmem_st_x4(taddr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int j = 0; j < NB_COLS; j += 4)
-        tmem_st_x4(taddr + 4 + j, b_cur[j], b_cur[j + 1], b_cur[j + 2], b_cur[j + 3]);
+      for (int j = 0; j < NB_COLS; j += 4) tmem_st_x4(taddr + 4 + j, b[j], b[j + 1], b[j + 2], b[j + 3]);
       tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + slot));
       ++gctr;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) a_cur[j] = a_nxt[j];
-#pragma unroll
-      for (int j = 0; j < NB_COLS; ++j) b_cur[j] = b_nxt[j];
-      t_cur = t_nxt;
-      kb_cur = kb_nxt;
-      tl_cur = tl_nxt;
+      advance(p);
+      advance(p);
+      if (p.t < num_tiles) load_words(p.tl, p.kb, a, b);
+      return true;
+    };
+    while (ok && p0.t < num_tiles) {
+      ok = write_group(p0, a0, b0);
+      if (!ok || p1.t >= num_tiles) break;
+      ok = write_group(p1, a1, b1);
     }
     aborted = !ok;
     }
