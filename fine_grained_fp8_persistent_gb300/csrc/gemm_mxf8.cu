@@ -15,7 +15,7 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
     }
   }
   switch (c.bn) {
-    case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 5>(a, tm, tiles, stream);
+    case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 4>(a, tm, tiles, stream);
     case 128: return launch_persistent<Kind::MXF8, S, 1, 128, 6>(a, tm, tiles, stream);
     case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 8>(a, tm, tiles, stream);
     default: return launch_persistent<Kind::MXF8, S, 1, 32, 8>(a, tm, tiles, stream);
@@ -38,9 +38,15 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta))
     return 4;
-  // the packed scale words are read by the kernel's scale-factor writers directly
-  (void)SFA;
-  (void)SFB;
+  // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
+  const long long kq = (a.K / 128 + 3) / 4;
+  const long long lda = (a.M + 3) / 4 * 4;
+  const long long ldn = (a.N + 3) / 4 * 4;
+  const long long sfa_rows = kq * (sched == Sched::Masked ? a.G : 1);
+  if (!encode_tmap_2d(&tm.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFA, lda, sfa_rows, lda * 4, 128, 1, false))
+    return 4;
+  if (!encode_tmap_2d(&tm.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, ldn, kq * a.G, ldn * 4, c.bn, 1, false))
+    return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {
     case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, stream);

@@ -18,10 +18,11 @@
 //            barrier (cp.async.bulk.tensor .cta_group::2).
 //   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).
 //   warps 2-5 (UE8M0 kernels) scale-factor writers, one per TMEM lane quarter:
-//            for each group of four K blocks they read the packed scale words
-//            from global memory and write them into a double-buffered TMEM slot
-//            with tcgen05.st (each quarter gets the same copy), then signal the
-//            MMA issuer (`sf_ready`, counted over the pair).  The block-scaled MMA
+//            one lane TMA-loads the packed scale words of each group of four K
+//            blocks into a small SMEM ring, three groups ahead; each writer reads
+//            them from there and writes them into a TMEM scale slot with
+//            tcgen05.st (each quarter gets the same copy), then signals the MMA
+//            issuer (`sf_ready`, counted over the pair).  The block-scaled MMA
 //            reads A's scale of row 32 j + l and B's scale of row 32 j + l from
 //            lane l, column j of its slot ("Blackwell Tensor Core: tcgen05.mma",
 //            Block-Scaled MMA: SFA/SFB live in TMEM).  Writing them from the
@@ -228,9 +229,14 @@ struct PCfg {
   // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
   // the per-K-block partials of the FP32-scale path (promotion latency slack).
   static constexpr int NACC = NACC_;
+  static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
+  static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
+  static constexpr int SFB_RING_BYTES = kMX ? SFB_ROWS * 4 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_BAR = (OFF_B + STAGES * B_BYTES + 7) / 8 * 8;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + SF_RING * SFA_RING_BYTES;
+  static constexpr int OFF_BAR = (OFF_SFB + SF_RING * SFB_RING_BYTES + 7) / 8 * 8;
   static constexpr int BAR_FULL = 0;
   static constexpr int BAR_EMPTY = STAGES;
   static constexpr int BAR_ACC_FULL = 2 * STAGES;                 // NACC
@@ -241,7 +247,9 @@ struct PCfg {
   static constexpr int SF_SLOTS = (2 * BN + 3 * SF_SLOT_COLS <= 512) ? 3 : 2;
   static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // SF_SLOTS: slot written (even CTA)
   static constexpr int BAR_SF_FREE = BAR_SFR + SF_SLOTS;          // SF_SLOTS: slot read (each CTA)
-  static constexpr int BAR_DRAIN = BAR_SF_FREE + SF_SLOTS;
+  static constexpr int BAR_SFL = BAR_SF_FREE + SF_SLOTS;          // SF_RING: words landed (local)
+  static constexpr int BAR_SFC = BAR_SFL + SF_RING;               // SF_RING: words read (local)
+  static constexpr int BAR_DRAIN = BAR_SFC + SF_RING;
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
@@ -259,6 +267,7 @@ struct PCfg {
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
   static_assert(NACC >= 2 && (kF32S || NACC == 2), "accumulator buffers");
+  static constexpr uint32_t SF_TX = BM * 4 + BN * 4;                // bytes landing on `sf_loaded`
 };
 
 __device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
@@ -333,6 +342,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       for (int b = 0; b < C::SF_SLOTS; ++b) {
         ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
         ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
+      }
+      for (int r = 0; r < C::SF_RING; ++r) {
+        ptx::mbar_init(bar(C::BAR_SFL + r), 1);
+        ptx::mbar_init(bar(C::BAR_SFC + r), C::SF_WARPS);
       }
     }
     ptx::mbar_init(bar(C::BAR_DRAIN), 1);
@@ -519,32 +532,12 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
     if constexpr (C::kMX) {
     ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
     const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp writes
-    const int ld_a = (M + 3) / 4 * 4;                  // rows of one activation table
-    const int ld_n = (N + 3) / 4 * 4;
+    const bool loader = warp == 2;                     // lane 0 of this warp issues the loads
     constexpr int NB_COLS = C::SFB_ROWS / 32;
-    // Column j of lane l holds the word of row 32 j + l (of this CTA's A rows, of
-    // the tile's B rows); rows outside the tables read as 0.
-    auto load_words = [&](const Tile& tl, int kb, uint32_t (&a)[4], uint32_t (&b)[NB_COLS]) {
-      const uint32_t* sfa_tab = args.sfa_ue8m0 +
-                                (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * kq * ld_a : 0) +
-                                static_cast<size_t>(kb / 4) * ld_a;
-      const uint32_t* sfb_tab = args.sfb_ue8m0 + (static_cast<size_t>(tl.group) * kq + kb / 4) * ld_n;
-      const int n0 = tl.n_blk * BN;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int m = tl.m_blk + 32 * j + static_cast<int>(lane);
-        a[j] = (m < ld_a) ? __ldg(sfa_tab + m) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < NB_COLS; ++j) {
-        const int r = 32 * j + static_cast<int>(lane);
-        b[j] = (r < BN && n0 + r < ld_n) ? __ldg(sfb_tab + n0 + r) : 0u;
-      }
-    };
-    // Walk (tile, group) in order with two register sets: while group g is
-    // written from one set, the words of group g + 1 are already in flight into
-    // the other (the loop is unrolled by two so that no register copy waits on
-    // an outstanding load).
+    if (loader && lane == 0) {
+      ptx::prefetch_tmap(&tm_sfa);
+      ptx::prefetch_tmap(&tm_sfb);
+    }
     auto next_valid = [&](int t, Tile& tl) -> int {
       for (; t < num_tiles; t += num_clusters)
         if (get_tile(t, tl)) return t;
@@ -558,22 +551,54 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
         p.t = next_valid(p.t + num_clusters, p.tl);
       }
     };
-    Pos p0, p1;
-    p0.kb = 0;
-    p0.t = next_valid(cluster_id, p0.tl);
-    p1 = p0;
-    advance(p1);
-    uint32_t a0[4], b0[NB_COLS], a1[4], b1[NB_COLS];
-    if (p0.t < num_tiles) load_words(p0.tl, p0.kb, a0, b0);
-    if (p1.t < num_tiles) load_words(p1.tl, p1.kb, a1, b1);
-    uint32_t gctr = 0;
+    // The loader keeps SF_RING - 1 groups in flight ahead of the writers.  A ring
+    // slot is reloaded once all four writers have read its previous group.
+    Pos pl;
+    pl.kb = 0;
+    pl.t = next_valid(cluster_id, pl.tl);
+    uint32_t gl = 0;
+    auto issue_load = [&]() -> bool {
+      const uint32_t r = gl % C::SF_RING;
+      const uint32_t round = gl / C::SF_RING;
+      if (round > 0 && !pwait(bar(C::BAR_SFC + r), (round - 1u) & 1u, ctl)) return false;
+      if (lane == 0) {
+        const uint32_t sfl = bar(C::BAR_SFL + r);
+        ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
+        const int sfa_row = (SCHED == Sched::Masked ? pl.tl.group * kq : 0) + pl.kb / 4;
+        ptx::tma_load_2d(sbase + C::OFF_SFA + r * C::SFA_RING_BYTES, &tm_sfa, sfl, pl.tl.m_blk, sfa_row);
+        ptx::tma_load_2d(sbase + C::OFF_SFB + r * C::SFB_RING_BYTES, &tm_sfb, sfl, pl.tl.n_blk * BN,
+                         pl.tl.group * kq + pl.kb / 4);
+      }
+      __syncwarp();
+      ++gl;
+      advance(pl);
+      return true;
+    };
     bool ok = true;
-    // write one group from (a, b), then refill (a, b) with the group two ahead
-    auto write_group = [&](Pos& p, uint32_t (&a)[4], uint32_t (&b)[NB_COLS]) -> bool {
+    if (loader)
+      for (int i = 0; ok && i < C::SF_RING - 1 && pl.t < num_tiles; ++i) ok = issue_load();
+    Pos pw;
+    pw.kb = 0;
+    pw.t = next_valid(cluster_id, pw.tl);
+    uint32_t gctr = 0;
+    while (ok && pw.t < num_tiles) {
+      if (loader && pl.t < num_tiles && !issue_load()) { ok = false; break; }
+      const uint32_t r = gctr % C::SF_RING;
+      if (!pwait(bar(C::BAR_SFL + r), (gctr / C::SF_RING) & 1u, ctl)) { ok = false; break; }
+      // word of row 32 j + l -> lane l, column j (rows past the tile are never read)
+      const uint32_t* sfa_s = reinterpret_cast<const uint32_t*>(smem + C::OFF_SFA + r * C::SFA_RING_BYTES);
+      const uint32_t* sfb_s = reinterpret_cast<const uint32_t*>(smem + C::OFF_SFB + r * C::SFB_RING_BYTES);
+      uint32_t a[4], b[NB_COLS];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a[j] = sfa_s[32 * j + lane];
+#pragma unroll
+      for (int j = 0; j < NB_COLS; ++j) b[j] = sfb_s[32 * j + lane];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::BAR_SFC + r));
       const uint32_t slot = gctr % C::SF_SLOTS;
       const uint32_t uses = gctr / C::SF_SLOTS;
-      // the slot was last read by group gctr - SF_SLOTS
-      if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) return false;
+      // the TMEM slot was last read by group gctr - SF_SLOTS
+      if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
       tmem_st_x4(taddr, a[0], a[1], a[2], a[3]);
@@ -584,15 +609,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_SFR + slot));
       ++gctr;
-      advance(p);
-      advance(p);
-      if (p.t < num_tiles) load_words(p.tl, p.kb, a, b);
-      return true;
-    };
-    while (ok && p0.t < num_tiles) {
-      ok = write_group(p0, a0, b0);
-      if (!ok || p1.t >= num_tiles) break;
-      ok = write_group(p1, a1, b1);
+      advance(pw);
     }
     aborted = !ok;
     }
