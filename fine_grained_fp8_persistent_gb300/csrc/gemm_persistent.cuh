@@ -57,9 +57,13 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+// Arrive on a barrier of any CTA of the cluster.  The default (release, CTA
+// scope) form is enough: what the waiting side reads next is either TMEM written
+// by tcgen05 ops this thread has already waited on (tcgen05.wait + fence pair) or
+// shared memory filled by TMA (counted in the barrier's transaction bytes).  A
+// cluster-scope release here costs on the order of a thousand cycles.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
@@ -160,17 +164,10 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Bounded wait with cluster-scope acquire (barriers that receive the peer's arrivals).
+// Test a phase of a barrier in this CTA (default acquire, CTA scope; see
+// mbar_arrive_cluster for why no cluster-scope ordering is needed).
 __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
+  return ptx::mbar_try_wait(bar, parity);
 }
 
 struct PairWaitCtl {
