@@ -13,14 +13,18 @@ namespace fgf8 {
 struct TileCfg {
   int ncta;   // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
   int bn;     // tile width
+  int npair;  // pairs per cluster sharing A by multicast (1 or 2)
 };
 
 // Tiles of the problem for a configuration (masked: upper bound, every expert full).
+// Tiles of the problem for a configuration, counted per cluster (masked: upper
+// bound, every expert full).
 inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
   const long long tm = 128LL * c.ncta;
   const long long mt = (a.M + tm - 1) / tm;
   const long long nt = (a.N + c.bn - 1) / c.bn;
-  return (s == Sched::Masked ? a.G : 1) * mt * nt;
+  const long long np = c.npair > 1 ? c.npair : 1;
+  return (s == Sched::Masked ? a.G : 1) * mt * ((nt + np - 1) / np);
 }
 
 // Estimated time of a configuration: waves of tiles over the SMs times the
@@ -29,22 +33,27 @@ inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
 // two SMs with half the B traffic per SM; it is credited 10 % for that.  Narrow
 // tiles spread skinny problems over more SMs (the DeepGEMM page's unaligned
 // BLOCK_N argument: 112 vs 128 blocks on 132 SMs).
-// FGF8_FORCE_TILE="<ncta>x<bn>" (e.g. "2x224") selects that configuration when it
-// is among the candidates (used by the tests to cover every instantiation).
+// FGF8_FORCE_TILE="<ctas per cluster>x<bn>" (e.g. "2x224", "4x224") selects that
+// configuration when it is among the candidates (used by the tests to cover
+// every instantiation).
 inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
   if (const char* f = std::getenv("FGF8_FORCE_TILE")) {
     int nc = 0, bn = 0;
     if (std::sscanf(f, "%dx%d", &nc, &bn) == 2)
       for (int i = 0; i < n; ++i)
-        if (cands[i].ncta == nc && cands[i].bn == bn) return i;
+        if (cands[i].ncta * (cands[i].npair > 1 ? cands[i].npair : 1) == nc && cands[i].bn == bn) return i;
   }
   const long long sms = device_sm_count();
   int best = 0;
   double best_cost = -1.0;
   for (int i = 0; i < n; ++i) {
-    const long long units = sms / cands[i].ncta;
+    const int cl = cands[i].ncta * (cands[i].npair > 1 ? cands[i].npair : 1);
+    const long long units = sms / cl;
     const long long waves = (tile_count(a, s, cands[i]) + units - 1) / units;
-    const double cost = static_cast<double>(waves) * (cands[i].bn + 32) * (cands[i].ncta == 2 ? 0.9 : 1.0);
+    // per-SM cost of one cluster tile; pairs halve each SM's B traffic and A
+    // multicast halves its A traffic (the L2 -> SMEM stream bounds these GEMMs)
+    const double share = cands[i].npair > 1 ? 0.75 : (cands[i].ncta == 2 ? 0.9 : 1.0);
+    const double cost = static_cast<double>(waves) * (cands[i].bn + 32) * (cl / cands[i].ncta) * share;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = i;
@@ -56,11 +65,12 @@ inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
 // Largest dynamic shared memory a CTA may opt into on sm_100-class parts (227 KB).
 constexpr int kMaxSmemOptin = 232448;
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2>
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, int NPAIR = 1>
 int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
   static_assert(C::SMEM_BYTES <= kMaxSmemOptin, "shared memory budget");
-  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC>;
+  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
+  constexpr int CL = C::CLUSTER;
   static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -71,7 +81,7 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = NCTA;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -83,19 +93,19 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return set_error(4, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     int clusters = 0;
-    cfg.gridDim = dim3(NCTA * device_sm_count(), 1, 1);
+    cfg.gridDim = dim3(CL * (device_sm_count() / CL), 1, 1);
     // the CTAs of a cluster are co-scheduled inside one GPC, so the number of pairs
     // that fit can be below SMs / 2 ("Dissecting NVIDIA Blackwell" (EEPW), section
     // on clusters, GPCs and die yield)
-    e = NCTA == 2 ? cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) : cudaSuccess;
-    if (NCTA == 1) clusters = device_sm_count();
+    e = CL > 1 ? cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) : cudaSuccess;
+    if (CL == 1) clusters = device_sm_count();
     if (e != cudaSuccess || clusters <= 0)
       return set_error(4, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
     max_clusters[dev] = clusters;
   }
   long long clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
   if (clusters < 1) clusters = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * NCTA), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, a);
   if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
   return 0;
@@ -104,10 +114,11 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
 // A and B operand maps: K-major rows of 128 bytes per stage, 128-byte swizzle;
 // each CTA loads 128 rows of A and BN / NCTA rows of B.
 inline int make_operand_maps(TensorMaps& tm, CUtensorMapDataType dt, int elem_bytes, const void* A,
-                             long long a_rows, const void* B, long long b_rows, int K, int b_box_rows) {
+                             long long a_rows, const void* B, long long b_rows, int K, int b_box_rows,
+                             int a_box_rows = 128) {
   std::memset(&tm, 0, sizeof(tm));
   const uint32_t bk = 128 / elem_bytes;
-  if (!encode_tmap_2d(&tm.a, dt, A, K, a_rows, static_cast<uint64_t>(K) * elem_bytes, bk, 128, true))
+  if (!encode_tmap_2d(&tm.a, dt, A, K, a_rows, static_cast<uint64_t>(K) * elem_bytes, bk, a_box_rows, true))
     return 4;
   if (!encode_tmap_2d(&tm.b, dt, B, K, b_rows, static_cast<uint64_t>(K) * elem_bytes, bk, b_box_rows,
                       true))

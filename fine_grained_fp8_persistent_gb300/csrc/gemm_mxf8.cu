@@ -8,6 +8,9 @@ namespace {
 template <Sched S>
 int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
                cudaStream_t stream) {
+  if constexpr (S == Sched::Dense) {
+    if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 7, 2, 2>(a, tm, tiles, stream);
+  }
   if constexpr (S != Sched::Contiguous) {
     if (c.ncta == 2) {
       if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 7>(a, tm, tiles, stream);
@@ -27,16 +30,18 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
                      const void* Bq, const void* SFB, cudaStream_t stream) {
   // the contiguous layout aligns expert segments to 128 rows: one CTA per tile
-  static const TileCfg pair_cands[] = {{2, 224}, {2, 128}, {1, 224}, {1, 128}, {1, 64}, {1, 32}};
-  static const TileCfg single_cands[] = {{1, 224}, {1, 128}, {1, 64}, {1, 32}};
-  const bool pairs = sched != Sched::Contiguous;
-  const TileCfg* cands = pairs ? pair_cands : single_cands;
-  const int n = pairs ? 6 : 4;
+  static const TileCfg dense_cands[] = {{2, 224, 2}, {2, 224, 1}, {2, 128, 1}, {1, 224, 1},
+                                        {1, 128, 1}, {1, 64, 1}, {1, 32, 1}};
+  static const TileCfg pair_cands[] = {{2, 224, 1}, {2, 128, 1}, {1, 224, 1}, {1, 128, 1}, {1, 64, 1}, {1, 32, 1}};
+  static const TileCfg single_cands[] = {{1, 224, 1}, {1, 128, 1}, {1, 64, 1}, {1, 32, 1}};
+  const TileCfg* cands = sched == Sched::Dense ? dense_cands : (sched == Sched::Masked ? pair_cands : single_cands);
+  const int n = sched == Sched::Dense ? 7 : (sched == Sched::Masked ? 6 : 4);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
   TensorMaps tm;
-  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta))
+  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
+                        128 / c.npair))
     return 4;
   // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
   const long long kq = (a.K / 128 + 3) / 4;

@@ -12,6 +12,14 @@
 // tile cuts both its SMEM footprint and its L2->SMEM traffic per FLOP by a third,
 // which leaves room for a deeper pipeline.
 //
+// With NPAIR = 2 a cluster holds two pairs working on adjacent N tiles of the
+// same 256 rows.  Both pairs need the same A rows, so each CTA loads half of its
+// A tile and multicasts it to its counterpart in the other pair (TMA
+// .multicast::cluster): the L2 -> SMEM traffic per pair and K block drops from
+// 2*(A + B/2) to 2*(A/2 + B/2).  That traffic, not the tensor pipe, is what
+// bounds this GEMM on GB300 (a pipeline of 7 stages in flight sees a ~2.5 us
+// load latency: bytes in flight divided by the L2 -> SM bandwidth).
+//
 // Roles (per CTA):
 //   warp 0   TMA producer: A/B tiles into a STAGES-deep ring of 128-byte-swizzled
 //            stages.  In a pair both CTAs' loads complete on the even CTA's `full`
@@ -83,6 +91,17 @@ __device__ __forceinline__ void tma_load_ab(uint32_t dst, const CUtensorMap* m, 
   }
 }
 
+// Load into this CTA's and the other pairs' shared memory at the same offset; the
+// transaction bytes land on each destination's pair-leader barrier.
+__device__ __forceinline__ void tma_load_mc_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
 // tcgen05 ops with the kernel-wide cta_group.
 template <int NCTA>
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -92,14 +111,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   else
     ptx::mma_commit(bar);
 }
-// Arrive on `bar` in every CTA of the pair once the tracked ops complete.
+// Arrive on `bar` in every CTA of `mask` once the tracked ops complete.
 template <int NCTA>
-__device__ __forceinline__ void tc_commit_all(uint32_t bar) {
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
   if constexpr (NCTA == 2)
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(bar),
-        "h"(static_cast<uint16_t>(3))
+        "h"(mask)
         : "memory");
   else
     ptx::mma_commit(bar);
@@ -198,9 +217,12 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2>
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
+  static constexpr int NPAIR = NPAIR_;               // pairs per cluster sharing A by multicast
+  static constexpr int CLUSTER = NCTA * NPAIR;
+  static_assert(NPAIR == 1 || (NPAIR == 2 && NCTA == 2 && SCHED == Sched::Dense), "A multicast");
   static constexpr int BM = 128;                    // rows per CTA
   static constexpr int TILE_M = BM * NCTA;
   static constexpr int BN = BN_;
@@ -215,6 +237,8 @@ struct PCfg {
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
   static constexpr int A_BYTES = BM * 128;
+  static constexpr int A_BOX_ROWS = BM / NPAIR;      // rows of A each CTA loads
+  static constexpr int A_BOX_BYTES = A_BOX_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
   static constexpr int SF_WARPS = kMX ? 4 : 0;
@@ -295,24 +319,30 @@ __device__ __forceinline__ void store_row32(void* D, size_t row_off, int col0, i
   }
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC>
-__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THREADS, 1)
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
-  const uint32_t rank = (NCTA == 2) ? cluster_rank() : 0u;
+  const uint32_t crank = (C::CLUSTER > 1) ? cluster_rank() : 0u;
+  const uint32_t rank = crank % NCTA;                 // rank within the pair
+  const uint32_t pair = crank / NCTA;                 // pair within the cluster
+  const uint32_t leader_rank = pair * NCTA;
   const bool leader = rank == 0;
+  // commit masks: this pair's CTAs, and every CTA of the cluster
+  const uint16_t pair_mask = static_cast<uint16_t>(((1u << NCTA) - 1u) << leader_rank);
+  const uint16_t all_mask = static_cast<uint16_t>((1u << C::CLUSTER) - 1u);
 
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
-  // the even CTA's copy of barrier i (cluster address)
-  auto lbar = [&](int i) -> uint32_t { return NCTA == 2 ? map_to_rank(bar(i), 0) : bar(i); };
+  // the pair leader's copy of barrier i (cluster address)
+  auto lbar = [&](int i) -> uint32_t { return NCTA == 2 ? map_to_rank(bar(i), leader_rank) : bar(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
@@ -322,14 +352,16 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
   const int num_n = (N + BN - 1) / BN;
   const int num_m = (M + C::TILE_M - 1) / C::TILE_M;   // per expert for masked
   const int kq = (K / 128 + 3) / 4;
-  const int cluster_id = static_cast<int>(blockIdx.x) / NCTA;
-  const int num_clusters = static_cast<int>(gridDim.x) / NCTA;
+  const int cluster_id = static_cast<int>(blockIdx.x) / C::CLUSTER;
+  const int num_clusters = static_cast<int>(gridDim.x) / C::CLUSTER;
+  const int num_nn = (num_n + NPAIR - 1) / NPAIR;     // N tiles per cluster tile row
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(bar(C::BAR_FULL + s), 1);
-      ptx::mbar_init(bar(C::BAR_EMPTY + s), 1);
+      // a stage is refilled once every pair that reads it has finished with it
+      ptx::mbar_init(bar(C::BAR_EMPTY + s), NPAIR);
     }
     for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
@@ -376,13 +408,13 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
     ptx::tc_fence_before();
   }
   __syncthreads();
-  if constexpr (NCTA == 2) cluster_sync_all();   // peer barriers initialised before any remote use
+  if constexpr (C::CLUSTER > 1) cluster_sync_all();   // peer barriers initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   int num_tiles;
   if constexpr (SCHED == Sched::Masked) num_tiles = prefix[G];
-  else num_tiles = num_m * num_n;
+  else num_tiles = num_m * num_nn;
 
   auto get_tile = [&](int t, Tile& tl) -> bool {
     int m, n, g = 0, rows;
@@ -400,7 +432,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
       n = local / mt;                              // M blocks sharing a B tile are adjacent
       m = local - n * mt;
     } else {
-      dense_tile(t, num_m, num_n, 16, m, n);
+      dense_tile(t, num_m, num_nn, 16, m, n);
+      n = n * NPAIR + static_cast<int>(pair);
       rows = M;
       if constexpr (SCHED == Sched::Contiguous) {
         g = __ldg(args.m_indices + m * C::TILE_M);
@@ -418,7 +451,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
   };
 
   PairWaitCtl ctl{abort_flag,
-                  NCTA == 2 ? map_to_rank(sbase + C::OFF_MISC + 4, rank ^ 1u) : 0u,
+                  NCTA == 2 ? map_to_rank(sbase + C::OFF_MISC + 4, crank ^ 1u) : 0u,
                   args.status, args.timeout_ns, 0};
   bool aborted = false;
 
@@ -440,7 +473,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
         if (lane == 0) {
           const uint32_t full = lbar(C::BAR_FULL + stage);
           if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
-          tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
+          if constexpr (NPAIR > 1) {
+            // this CTA's share of the A tile, into the same rows of every pair
+            const uint16_t mask = static_cast<uint16_t>(((1u << rank) | (1u << (rank + NCTA))));
+            tma_load_mc_pair(sbase + C::OFF_A + stage * C::A_BYTES + pair * C::A_BOX_BYTES, &tm_a, full,
+                             kb * C::BK, tl.a_row0 + static_cast<int>(pair) * C::A_BOX_ROWS, mask);
+          } else {
+            tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
+          }
           tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
         }
         __syncwarp();
@@ -492,11 +532,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
               const uint32_t accum = C::kF32S ? (k > 0 ? 1u : 0u) : ((kb > 0 || k > 0) ? 1u : 0u);
               tc_mma<NCTA, KIND>(d_tmem, ad, bd, id, sf_col, sf_col + 4, accum);
             }
-            tc_commit_all<NCTA>(bar(C::BAR_EMPTY + stage));
+            tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + stage), all_mask);
             if constexpr (C::kMX) {
-              if (kb % 4 == 3 || kb == nkb - 1) tc_commit_all<NCTA>(bar(C::BAR_SF_FREE + slot));
+              if (kb % 4 == 3 || kb == nkb - 1) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + slot), pair_mask);
             }
-            if constexpr (C::kF32S) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
+            if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
           }
           __syncwarp();
           if constexpr (C::kMX) {
@@ -509,7 +549,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
         }
         if (!ok) break;
         if constexpr (!C::kF32S) {
-          if (lane == 0) tc_commit_all<NCTA>(bar(C::BAR_ACC_FULL + acc));
+          if (lane == 0) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
           __syncwarp();
           if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
         }
@@ -735,7 +775,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC>::THR
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if constexpr (NCTA == 2) cluster_sync_all();
+  if constexpr (C::CLUSTER > 1) cluster_sync_all();
   if (warp == 1) {
     ptx::tc_fence_after();
     tc_dealloc<NCTA>(tmem_base, C::TMEM_ALLOC);

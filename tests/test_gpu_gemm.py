@@ -120,14 +120,15 @@ def test_host_validation_errors(fg, dev):
 
 
 # Every tile configuration the launchers can pick, forced through FGF8_FORCE_TILE
-# (one CTA per tile, or a CTA pair with M = 256 and B split across the pair).
-MXF8_TILES = ["2x224", "2x128", "1x224", "1x128", "1x64", "1x32"]
+# as "<CTAs per cluster>x<BN>": one CTA per tile, a CTA pair (M = 256, B split
+# across the pair), or two pairs sharing A by TMA multicast.
+MXF8_TILES = ["4x224", "2x224", "2x128", "1x224", "1x128", "1x64", "1x32"]
 F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
-F16_TILES = ["2x256", "1x128"]
+F16_TILES = ["4x256", "2x256", "1x128"]
 
 
 @pytest.mark.parametrize("tile", MXF8_TILES)
-@pytest.mark.parametrize("M,N,K", [(384, 448, 640), (130, 96, 512)])
+@pytest.mark.parametrize("M,N,K", [(384, 448, 640), (130, 96, 512), (300, 672, 512)])
 def test_fp8_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     case = _fp8_case(M, N, K, 1, 300 + M)
@@ -145,7 +146,7 @@ def test_fp8_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
 
 
 @pytest.mark.parametrize("tile", F16_TILES)
-@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200)])
+@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200), (520, 768, 256)])
 def test_f16_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     a = inputs.uniform_16bit((M, K), 500 + M, dtype=torch.bfloat16)
