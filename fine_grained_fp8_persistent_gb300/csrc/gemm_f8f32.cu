@@ -23,8 +23,9 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
                       cudaStream_t stream) {
-  static const TileCfg pair_cands[] = {{2, 128, 1}, {1, 256, 1}, {1, 128, 1}, {1, 64, 1}};
-  static const TileCfg single_cands[] = {{1, 256, 1}, {1, 128, 1}, {1, 64, 1}};
+  // relative tile times: see pick_cfg (the 64 width is extrapolated)
+  static const TileCfg pair_cands[] = {{2, 128, 1, 23.4}, {1, 256, 1, 36.1}, {1, 128, 1, 23.6}, {1, 64, 1, 14.0}};
+  static const TileCfg single_cands[] = {{1, 256, 1, 36.1}, {1, 128, 1, 23.6}, {1, 64, 1, 14.0}};
   const bool pairs = sched != Sched::Contiguous;
   const TileCfg* cands = pairs ? pair_cands : single_cands;
   const int n = pairs ? 4 : 3;

@@ -11,12 +11,12 @@ namespace fgf8 {
 
 // One kernel configuration the launchers can choose from.
 struct TileCfg {
-  int ncta;   // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
-  int bn;     // tile width
-  int npair;  // pairs per cluster sharing A by multicast (1 or 2)
+  int ncta;       // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
+  int bn;         // tile width
+  int npair;      // pairs per cluster sharing A by multicast (1 or 2)
+  double t_tile;  // relative time of one cluster tile (measured, see pick_cfg)
 };
 
-// Tiles of the problem for a configuration (masked: upper bound, every expert full).
 // Tiles of the problem for a configuration, counted per cluster (masked: upper
 // bound, every expert full).
 inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
@@ -27,12 +27,13 @@ inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
   return (s == Sched::Masked ? a.G : 1) * mt * ((nt + np - 1) / np);
 }
 
-// Estimated time of a configuration: waves of tiles over the SMs times the
-// per-tile cost (BN + 32: the 32 stands for the work that does not scale with
-// BN: the A tile, the epilogue drain).  A pair tile computes twice the rows on
-// two SMs with half the B traffic per SM; it is credited 10 % for that.  Narrow
-// tiles spread skinny problems over more SMs (the DeepGEMM page's unaligned
-// BLOCK_N argument: 112 vs 128 blocks on 132 SMs).
+// Estimated time of a configuration: waves of cluster tiles over the SMs times the
+// time of one cluster tile.  The tile times are measured on a GB300 at M = 4096,
+// N = K = 7168 (microseconds per tile, the same K for every candidate, so only
+// their ratios matter); the widths not measured there are extrapolated from the
+// narrowest measured ones.  A wide tile wins on large problems; narrow tiles spread
+// skinny problems over more SMs (the DeepGEMM page's unaligned BLOCK_N argument:
+// 112 vs 128 blocks on 132 SMs).
 // FGF8_FORCE_TILE="<ctas per cluster>x<bn>" (e.g. "2x224", "4x224") selects that
 // configuration when it is among the candidates (used by the tests to cover
 // every instantiation).
@@ -50,10 +51,7 @@ inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
     const int cl = cands[i].ncta * (cands[i].npair > 1 ? cands[i].npair : 1);
     const long long units = sms / cl;
     const long long waves = (tile_count(a, s, cands[i]) + units - 1) / units;
-    // per-SM cost of one cluster tile; pairs halve each SM's B traffic and A
-    // multicast halves its A traffic (the L2 -> SMEM stream bounds these GEMMs)
-    const double share = cands[i].npair > 1 ? 0.75 : (cands[i].ncta == 2 ? 0.9 : 1.0);
-    const double cost = static_cast<double>(waves) * (cands[i].bn + 32) * (cl / cands[i].ncta) * share;
+    const double cost = static_cast<double>(waves) * cands[i].t_tile;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = i;

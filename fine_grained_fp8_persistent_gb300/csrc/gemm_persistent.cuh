@@ -241,10 +241,18 @@ struct PCfg {
   static constexpr int A_BOX_BYTES = A_BOX_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
+  // K blocks per pipeline unit: one full/empty handshake, one hand-off to the MMA
+  // warp and one commit per unit.  The FP32-scale path hands every K block's
+  // partial product to the promotion warps, so its unit is one K block.
+  static constexpr int KPU = kF32S ? 1 : 2;
+  static_assert(STAGES % KPU == 0, "stages per unit");
+  static constexpr int UNITS = STAGES / KPU;
   static constexpr int SF_WARPS = kMX ? 4 : 0;
   static constexpr int EPI_WARPS = kF32S ? 8 : 4;
   static constexpr int EPI_WARP0 = 2 + SF_WARPS;
-  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr int RELAY_WARP = EPI_WARP0 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (RELAY_WARP + 1);
+  static constexpr int HANDOFF_BAR = 1;              // named barrier: relay warp + MMA warp
   static constexpr int MAX_GROUPS = 1024;
 
   // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
@@ -258,9 +266,9 @@ struct PCfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + SF_RING * SFA_RING_BYTES;
   static constexpr int OFF_BAR = (OFF_SFB + SF_RING * SFB_RING_BYTES + 7) / 8 * 8;
-  static constexpr int BAR_FULL = 0;
-  static constexpr int BAR_EMPTY = STAGES;
-  static constexpr int BAR_ACC_FULL = 2 * STAGES;                 // NACC
+  static constexpr int BAR_FULL = 0;                              // UNITS
+  static constexpr int BAR_EMPTY = UNITS;                         // UNITS
+  static constexpr int BAR_ACC_FULL = 2 * UNITS;                  // NACC
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + NACC;       // NACC
   // TMEM scale slots: three where they fit next to the accumulators, so the
   // scale writers can run two groups of K blocks ahead of the MMA
@@ -290,6 +298,15 @@ struct PCfg {
   static_assert(NACC >= 2 && (kF32S || NACC == 2), "accumulator buffers");
   static constexpr uint32_t SF_TX = BM * 4 + BN * 4;                // bytes landing on `sf_loaded`
 };
+
+// Named-barrier rendezvous of `nthreads` threads (whole warps).  It goes through the
+// CTA barrier unit, not shared memory: the MMA warp waits here instead of polling an
+// mbarrier, because a shared-memory access by the thread that issues tcgen05.mma
+// queues behind its pending MMAs (measured: ~170 cycles for a try_wait on a
+// completed barrier, 43 from any other warp).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
   if (bf16) {
@@ -358,10 +375,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(bar(C::BAR_FULL + s), 1);
-      // a stage is refilled once every pair that reads it has finished with it
-      ptx::mbar_init(bar(C::BAR_EMPTY + s), NPAIR);
+    for (int u = 0; u < C::UNITS; ++u) {
+      ptx::mbar_init(bar(C::BAR_FULL + u), 1);
+      // a unit is refilled once every pair that reads it has finished with it
+      ptx::mbar_init(bar(C::BAR_EMPTY + u), NPAIR);
     }
     for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
@@ -462,99 +479,102 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       ptx::prefetch_tmap(&tm_a);
       ptx::prefetch_tmap(&tm_b);
     }
-    int stage = 0;
+    int unit = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
       Tile tl;
       if (!get_tile(t, tl)) continue;
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!pwait(bar(C::BAR_EMPTY + stage), phase ^ 1u, ctl)) { ok = false; break; }
+      for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
+        if (!pwait(bar(C::BAR_EMPTY + unit), phase ^ 1u, ctl)) { ok = false; break; }
         if (lane == 0) {
-          const uint32_t full = lbar(C::BAR_FULL + stage);
-          if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + stage), C::A_TX);
-          if constexpr (NPAIR > 1) {
-            // this CTA's share of the A tile, into the same rows of every pair
-            const uint16_t mask = static_cast<uint16_t>(((1u << rank) | (1u << (rank + NCTA))));
-            tma_load_mc_pair(sbase + C::OFF_A + stage * C::A_BYTES + pair * C::A_BOX_BYTES, &tm_a, full,
-                             kb * C::BK, tl.a_row0 + static_cast<int>(pair) * C::A_BOX_ROWS, mask);
-          } else {
-            tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
+          const int nk = min(C::KPU, nkb - kb0);     // K blocks in this unit (the tail may be short)
+          const uint32_t full = lbar(C::BAR_FULL + unit);
+          if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + unit), static_cast<uint32_t>(nk) * C::A_TX);
+          for (int j = 0; j < nk; ++j) {
+            const int stage = unit * C::KPU + j;
+            const int kb = kb0 + j;
+            if constexpr (NPAIR > 1) {
+              // this CTA's share of the A tile, into the same rows of every pair
+              const uint16_t mask = static_cast<uint16_t>(((1u << rank) | (1u << (rank + NCTA))));
+              tma_load_mc_pair(sbase + C::OFF_A + stage * C::A_BYTES + pair * C::A_BOX_BYTES, &tm_a, full,
+                               kb * C::BK, tl.a_row0 + static_cast<int>(pair) * C::A_BOX_ROWS, mask);
+            } else {
+              tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
+            }
+            tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
           }
-          tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
         }
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (++unit == C::UNITS) { unit = 0; phase ^= 1u; }
       }
     }
     aborted = !ok;
   } else if (warp == 1) {
     // ============================================================ MMA issuer
+    // Issues straight from a named-barrier hand-off: the relay warp has already
+    // waited for everything the unit needs, so this warp touches no shared memory
+    // between MMAs and the tensor pipe never runs dry between units.
     ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
     if (leader) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int unit = 0;
       int acc = 0;
-      uint32_t acc_phase = 0;
       uint32_t gctr = 0u;            // scale-word groups consumed so far (all tiles)
-      bool ok = true;
       const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
-      const uint32_t idesc_plain = idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
-      for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+      const uint32_t idesc0 = C::kMX ? idesc_mxf8(BN, C::TILE_M, 0, 0) : idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
+      // descriptors are linear in the address (start field = address >> 4)
+      const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
+      const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
+      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
         Tile tl;
         if (!get_tile(t, tl)) continue;
-        if constexpr (!C::kF32S) {
-          if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
-        }
-        uint32_t slot = 0;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!pwait(bar(C::BAR_FULL + stage), phase, ctl)) { ok = false; break; }
-          if constexpr (C::kF32S) {
-            if (!pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl)) { ok = false; break; }
-          }
-          if (C::kMX && kb % 4 == 0) {
-            // the scale writers filled this group's slot
-            slot = gctr % C::SF_SLOTS;
-            if (!pwait(bar(C::BAR_SFR + slot), (gctr / C::SF_SLOTS) & 1u, ctl)) { ok = false; break; }
-          }
+        uint32_t sf_col = 0;
+        for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
+          named_bar_sync(C::HANDOFF_BAR, 64);
           ptx::tc_fence_after();
+          const int nk = min(C::KPU, nkb - kb0);
+          const int kl = kb0 + nk - 1;                   // last K block of the unit
+          const bool group_end = C::kMX && (kl % 4 == 3 || kl == nkb - 1);
           if (lane == 0) {
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-            const uint32_t sf_col = tmem_base + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-            const uint32_t a0 = sbase + C::OFF_A + stage * C::A_BYTES;
-            const uint32_t b0 = sbase + C::OFF_B + stage * C::B_BYTES;
-#pragma unroll
-            for (int k = 0; k < C::MMAS_PER_STAGE; ++k) {
-              const uint64_t ad = smem_desc_sw128(a0 + k * C::MMA_K_BYTES);
-              const uint64_t bd = smem_desc_sw128(b0 + k * C::MMA_K_BYTES);
-              uint32_t id = idesc_plain;
-              if constexpr (C::kMX) id = idesc_mxf8(BN, C::TILE_M, kb % 4, kb % 4);
-              const uint32_t accum = C::kF32S ? (k > 0 ? 1u : 0u) : ((kb > 0 || k > 0) ? 1u : 0u);
-              tc_mma<NCTA, KIND>(d_tmem, ad, bd, id, sf_col, sf_col + 4, accum);
-            }
-            tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + stage), all_mask);
             if constexpr (C::kMX) {
-              if (kb % 4 == 3 || kb == nkb - 1) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + slot), pair_mask);
+              if (kb0 % 4 == 0) sf_col = tmem_base + C::SF_COL0 + (gctr % C::SF_SLOTS) * C::SF_SLOT_COLS;
             }
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+#pragma unroll
+            for (int j = 0; j < C::KPU; ++j) {
+              if (j < nk) {
+                const int kb = kb0 + j;
+                const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
+                const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
+                const uint64_t bd = bdesc0 + stage * (C::B_BYTES >> 4);
+                // block-scaled: byte kb % 4 of each scale word (a_sf_id, b_sf_id)
+                const uint32_t sfid = static_cast<uint32_t>(kb & 3);
+                const uint32_t id = C::kMX ? (idesc0 | (sfid << 4) | (sfid << 29)) : idesc0;
+#pragma unroll
+                for (int k = 0; k < C::MMAS_PER_STAGE; ++k) {
+                  const uint32_t accum = C::kF32S ? (k > 0 ? 1u : 0u) : ((kb > 0 || k > 0) ? 1u : 0u);
+                  tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), id,
+                                     sf_col, sf_col + 4, accum);
+                }
+              }
+            }
+            tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + unit), all_mask);
+            if (group_end) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + gctr % C::SF_SLOTS), pair_mask);
             if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
           }
           __syncwarp();
-          if constexpr (C::kMX) {
-            if (kb % 4 == 3 || kb == nkb - 1) ++gctr;
-          }
+          if (group_end) ++gctr;
           if constexpr (C::kF32S) {
-            if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == C::NACC) acc = 0;
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++unit == C::UNITS) unit = 0;
         }
-        if (!ok) break;
         if constexpr (!C::kF32S) {
           if (lane == 0) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
           __syncwarp();
-          if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+          if (++acc == C::NACC) acc = 0;
         }
       }
-      aborted = !ok;
       // every tcgen05 op issued completes before TMEM is released
       if (lane == 0) tc_commit<NCTA>(bar(C::BAR_DRAIN));
       __syncwarp();
@@ -649,6 +669,50 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       advance(pw);
     }
     aborted = !ok;
+    }
+  } else if (warp == C::RELAY_WARP) {
+    // ============================================================ relay
+    // Waits, for the MMA warp, on everything a unit of MMAs needs (operands landed,
+    // accumulator drained by the epilogue, scale slot written) and then meets it at
+    // the named barrier; both walk the same schedule of units.  After a failed wait
+    // it keeps meeting the barrier without waiting, so the MMA warp always finishes
+    // its schedule (on stale data; the status word reports the failure).
+    ctl.role_bit = FGF8_DEVERR_ROLE_MMA;
+    if (leader) {
+      int unit = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      uint32_t gctr = 0u;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        Tile tl;
+        if (!get_tile(t, tl)) continue;
+        if constexpr (!C::kF32S) {
+          if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
+        }
+        for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
+          if constexpr (C::kF32S) {
+            if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
+          }
+          if constexpr (C::kMX) {
+            if (ok && kb0 % 4 == 0)
+              ok = pwait(bar(C::BAR_SFR + gctr % C::SF_SLOTS), (gctr / C::SF_SLOTS) & 1u, ctl);
+          }
+          if (ok) ok = pwait(bar(C::BAR_FULL + unit), phase, ctl);
+          named_bar_sync(C::HANDOFF_BAR, 64);
+          const int kl = min(kb0 + C::KPU, nkb) - 1;
+          if (C::kMX && (kl % 4 == 3 || kl == nkb - 1)) ++gctr;
+          if constexpr (C::kF32S) {
+            if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+          }
+          if (++unit == C::UNITS) { unit = 0; phase ^= 1u; }
+        }
+        if constexpr (!C::kF32S) {
+          if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+        }
+      }
+      aborted = !ok;
     }
   } else if constexpr (!C::kF32S) {
     // ============================================================ epilogue
