@@ -17,7 +17,6 @@ workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -37,13 +36,18 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of the GEMM kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch), valid only for the kernel sources it was
-# taken from (sha256 over csrc/).  See profiles/.
-NCU_TRAFFIC = {"src_sha": None, "bytes_per_launch": None}
+# taken from (sha256 over GEMM_SOURCES).  See profiles/.
+NCU_TRAFFIC = {"src_sha": "9b7ecf08c4bd7321", "bytes_per_launch": 144603136}
+
+
+# sources the block-scaled GEMM kernel and its launch are compiled from
+GEMM_SOURCES = ("api.cu", "device_common.cuh", "fgf8_internal.h", "gemm_launch.cuh", "gemm_mxf8.cu",
+                "gemm_persistent.cuh", "ptx.cuh")
 
 
 def _src_sha() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "fine_grained_fp8_persistent_gb300", "csrc", "*"))):
+    for p in [os.path.join(ROOT, "fine_grained_fp8_persistent_gb300", "csrc", f) for f in GEMM_SOURCES]:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
@@ -200,6 +204,7 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
+    gemm_tile = fg.last_tile()
     if world > 1:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -249,7 +254,7 @@ def run_ours(args) -> None:
                          "traffic": traffic,
                          "peak_note": f"FP8 dense = 2 x bf16 burst GEMM peak ({bf16_peak} TFLOP/s, {src}); "
                                       f"vs sustained: {round(achieved / (2 * bf16_sust), 4)}",
-                         "kernel": "gemm_kernel<MXF8, Dense, 224, 4>"},
+                         "kernel": f"gemm_persistent ({gemm_tile})"},
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,
@@ -373,10 +378,17 @@ def _oracle_sample(rows: int):
     return time.perf_counter() - t0, 2.0 * rows * N_OUT * K_IN
 
 
+def _sample_rows(seconds: float) -> int:
+    """Output rows of one oracle sample that takes about `seconds` on this host
+    (calibrated on an 8-row sample)."""
+    t8, _ = _oracle_sample(8)
+    return int(max(1, min(M_TOK, round(8 * seconds / max(t8, 1e-3)))))
+
+
 def _cpu_baseline(args) -> dict:
     import oracle
     oracle.build()
-    rows = args.cpu_rows
+    rows = args.cpu_rows if args.cpu_rows > 0 else _sample_rows(args.cpu_seconds)
     secs, flops = _oracle_sample(rows)
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
@@ -391,7 +403,10 @@ def run_reference(args) -> None:
         return
     import oracle
     oracle.build()
-    rows = args.cpu_rows
+    # each step is a bounded sample, sized so the whole run takes about
+    # --ref-seconds on the host cores
+    rows = args.cpu_rows if args.cpu_rows > 0 else \
+        _sample_rows(args.ref_seconds / (args.steps + args.warmup))
     for _ in range(args.warmup):
         _oracle_sample(rows)
     tot = 0.0
@@ -424,10 +439,13 @@ def run_reference(args) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=8, help="output rows in one oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="output rows in one oracle sample (0: sized from --cpu-seconds / --ref-seconds)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the cpu_baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=120.0, help="target length of an --impl reference run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-variants", action="store_true", help="skip the extra kernel lines")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")

@@ -54,6 +54,7 @@ _SIGS = {
     "fgf8_sfb_bytes": ([_I, _I, _I, _I], _LL),
     "fgf8_check_status": ([_P, ctypes.POINTER(ctypes.c_uint)], _I),
     "fgf8_last_error": ([], ctypes.c_char_p),
+    "fgf8_last_tile": ([], ctypes.c_char_p),
     "fgf8_set_wait_timeout_ms": ([_I], _I),
     "fgf8_version": ([], _I),
 }
@@ -227,6 +228,11 @@ def sfa_bytes(rows: int, K: int, fmt) -> int:
 
 def sfb_bytes(G: int, N: int, K: int, fmt) -> int:
     return int(_lib.fgf8_sfb_bytes(G, N, K, _fmt(fmt)))
+
+
+def last_tile() -> str:
+    """Kernel configuration of the last GEMM this thread launched ("mxf8 dense 2x224")."""
+    return (_lib.fgf8_last_tile() or b"").decode()
 
 
 def set_wait_timeout_ms(ms: int) -> int:

@@ -21,6 +21,7 @@ constexpr int kMaxGroups = 1024; // masked scheduler keeps a per-expert prefix i
 __device__ uint32_t g_status;
 
 thread_local char g_errbuf[512];
+thread_local char g_last_tile[64];
 
 struct DevInfo {
   bool ready = false;
@@ -71,6 +72,10 @@ long long align4(long long x) { return (x + 3) / 4 * 4; }
 }  // namespace
 
 namespace fgf8 {
+
+void set_last_tile(const char* kind, const char* sched, int ctas, int bn) {
+  std::snprintf(g_last_tile, sizeof(g_last_tile), "%s %s %dx%d", kind, sched, ctas, bn);
+}
 
 int set_error(int code, const char* fmt, ...) {
   va_list ap;
@@ -147,6 +152,8 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 extern "C" {
 
 const char* fgf8_last_error(void) { return g_errbuf; }
+
+const char* fgf8_last_tile(void) { return g_last_tile; }
 
 int fgf8_version(void) { return 100; }
 

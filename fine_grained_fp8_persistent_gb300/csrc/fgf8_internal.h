@@ -44,6 +44,8 @@ struct TensorMaps {
 
 // Host helpers (host.cu).
 int set_error(int code, const char* fmt, ...);
+// Records the configuration of the GEMM launch this thread makes (fgf8_last_tile).
+void set_last_tile(const char* kind, const char* sched, int ctas, int bn);
 int device_sm_count();
 int device_max_smem_optin();
 uint32_t* device_status_ptr();

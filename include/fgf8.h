@@ -176,6 +176,12 @@ FGF8_API int fgf8_check_status(void* stream, unsigned int* raw_bits);
 /* Message for the last non-OK return on this thread ("" if none). */
 FGF8_API const char* fgf8_last_error(void);
 
+/* Kernel configuration of the last GEMM this thread launched, as text
+ * ("<kind> <schedule> <CTAs per cluster>x<tile width>", e.g. "mxf8 dense 2x224");
+ * "" before the first launch.  The pointer stays valid until this thread's next
+ * GEMM call. */
+FGF8_API const char* fgf8_last_tile(void);
+
 /* Upper bound, in milliseconds, on any single pipeline wait inside a kernel
  * (default 2000; also read from the environment variable FGF8_WAIT_TIMEOUT_MS
  * at first use).  Returns the previous value. */

@@ -133,6 +133,7 @@ def test_fp8_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     case = _fp8_case(M, N, K, 1, 300 + M)
     out = _run_fp8(fg, dev, case, 1, M, N)
+    assert fg.last_tile() == f"mxf8 dense {tile}"
     gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 1), f"ue8m0 {tile} {M}x{N}x{K}")
 
 
@@ -142,11 +143,13 @@ def test_fp8_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     case = _fp8_case(M, N, K, 0, 400 + M)
     out = _run_fp8(fg, dev, case, 0, M, N)
+    assert fg.last_tile() == f"f8f32 dense {tile}"
     gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 0), f"f32 {tile} {M}x{N}x{K}")
 
 
 @pytest.mark.parametrize("tile", F16_TILES)
-@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200), (520, 768, 256)])
+# K = 136 and 200 leave a short last K block; 136 also gives an odd count of K blocks
+@pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200), (520, 768, 256), (200, 256, 136)])
 def test_f16_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     a = inputs.uniform_16bit((M, K), 500 + M, dtype=torch.bfloat16)
@@ -154,5 +157,6 @@ def test_f16_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     out = fg.gemm_f16(a.to(dev), b.to(dev))
     rc, _ = fg.check_status()
     assert rc == 0
+    assert fg.last_tile() == f"f16 dense {tile}"
     gemm_close(out.float().cpu().numpy(), oracle.gemm_f16(a.float().numpy(), b.float().numpy()),
                f"f16 {tile} {M}x{N}x{K}")
