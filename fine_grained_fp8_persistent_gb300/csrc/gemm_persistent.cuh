@@ -16,31 +16,44 @@
 // same 256 rows.  Both pairs need the same A rows, so each CTA loads half of its
 // A tile and multicasts it to its counterpart in the other pair (TMA
 // .multicast::cluster): the L2 -> SMEM traffic per pair and K block drops from
-// 2*(A + B/2) to 2*(A/2 + B/2).  That traffic, not the tensor pipe, is what
-// bounds this GEMM on GB300 (a pipeline of 7 stages in flight sees a ~2.5 us
-// load latency: bytes in flight divided by the L2 -> SM bandwidth).
+// 2*(A + B/2) to 2*(A/2 + B/2).  Measured on GB300 this variant is slower than
+// the plain pair (the four-CTA cluster spreads worse over the GPCs and the
+// L2 -> SMEM stream is not the bound), so the launchers only take it when forced.
+//
+// Pipeline unit.  The producer fills, and the MMA warp consumes, KPU K blocks
+// (two, one for the FP32-scale path) per full/empty handshake, so one hand-off
+// covers 8 MMAs.
 //
 // Roles (per CTA):
 //   warp 0   TMA producer: A/B tiles into a STAGES-deep ring of 128-byte-swizzled
 //            stages.  In a pair both CTAs' loads complete on the even CTA's `full`
 //            barrier (cp.async.bulk.tensor .cta_group::2).
-//   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).
+//   warp 1   MMA issuer (even CTA; one thread) and TMEM owner (both CTAs).  It
+//            never polls an mbarrier: it meets the relay warp at a named barrier
+//            and then issues the unit's MMAs and commits back to back.  An
+//            mbarrier try_wait (or any shared-memory access) by the thread that
+//            issues tcgen05.mma queues behind its pending MMAs, ~170 cycles even on
+//            a completed barrier, which starved the tensor pipe between units.
 //   warps 2-5 (UE8M0 kernels) scale-factor writers, one per TMEM lane quarter:
 //            one lane TMA-loads the packed scale words of each group of four K
 //            blocks into a small SMEM ring, three groups ahead; each writer reads
 //            them from there and writes them into a TMEM scale slot with
-//            tcgen05.st (each quarter gets the same copy), then signals the MMA
-//            issuer (`sf_ready`, counted over the pair).  The block-scaled MMA
-//            reads A's scale of row 32 j + l and B's scale of row 32 j + l from
-//            lane l, column j of its slot ("Blackwell Tensor Core: tcgen05.mma",
+//            tcgen05.st (each quarter gets the same copy), then signals
+//            `sf_ready` (counted over the pair).  The block-scaled MMA reads A's
+//            scale of row 32 j + l and B's scale of row 32 j + l from lane l,
+//            column j of its slot ("Blackwell Tensor Core: tcgen05.mma",
 //            Block-Scaled MMA: SFA/SFB live in TMEM).  Writing them from the
 //            warps keeps the copy out of the tensor pipe: a tcgen05.cp issued
 //            between MMAs stalls the MMA stream for several hundred cycles.
-//   rest     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
+//   next     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
 //            promotion (8 warps: per-128-K partial from TMEM, acc += sA*sB*partial
 //            on the CUDA cores, the DeepGEMM page's promotion loop).
+//   last     relay warp (even CTA): waits, for the MMA warp, on the unit's `full`
+//            barrier, the accumulator's `empty` barrier and the scale slot's
+//            `sf_ready`, then meets the MMA warp at the named barrier.
 // Pipeline handshakes follow the tma2mma / mma2tma / mma2ld / ld2mma barriers of
-// "TIRx and high-performance GEMM (part 2)" (Steps 7-8); every wait is bounded.
+// "TIRx and high-performance GEMM (part 2)" (Steps 7-8); every mbarrier wait is
+// bounded.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
