@@ -161,6 +161,23 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(value: float, world: int, device) -> float:
+    """Largest `value` over all ranks (the slowest rank's time sets the job's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_tflops(steps: int, world: int, t_max_ms: float) -> float:
+    """Whole-job throughput: each of `world` ranks ran `steps` steps of its own
+    batch (weak scaling) in at most `t_max_ms`."""
+    return FLOPS_PER_STEP * steps * world / (t_max_ms * 1e-3) / 1e12
+
+
 # ============================================================================ ours
 def run_ours(args) -> None:
     import torch
@@ -238,11 +255,8 @@ def run_ours(args) -> None:
     if rc != 0:
         raise RuntimeError(f"device status {rc} bits {bits:#x} after the timed steps")
 
-    t_local = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    t_max_ms = float(t_local.item())
-    value = FLOPS_PER_STEP * args.steps * world / (t_max_ms * 1e-3) / 1e12
+    t_max_ms = _max_over_ranks(total_ms, world, dev)
+    value = _job_tflops(args.steps, world, t_max_ms)
 
     e2e = None if args.no_e2e else _e2e(args, fg, x_cpu, w_cpu, dev, stream)
     variants = _variants(fg, dev, stream) if rank == 0 and not args.no_variants else None
