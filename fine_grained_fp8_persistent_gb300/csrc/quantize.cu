@@ -7,9 +7,9 @@
 // power-of-two (UE8M0) scales, the exponent is rounded up so nothing saturates.
 //
 // Both kernels are HBM-bound streams: 2 bytes read and 1 byte written per
-// element plus the small scale tables.  Loads are 16-byte vectors, each warp
-// covers a contiguous 1 KB (1x128) or 256 B row segments (128x128), and the
-// packed UE8M0 words are assembled on chip so each scale word is written once.
+// element plus the small scale tables, each input byte read once.  Loads are
+// 16-byte vectors; a warp covers a contiguous 1 KB (1x128) or two 256-byte row
+// segments (128x128).
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -69,18 +69,45 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], bool f32_scale, flo
   return r;
 }
 
-// One warp per (row m, group of four 128-wide K blocks); each warp handles two
-// such items per iteration with all four 16-byte loads in flight before any
-// arithmetic.  Lane l covers elements [16 l, 16 l + 16) of a 512-element chunk,
-// so lanes 8j..8j+7 own K block j of the group.
-constexpr int kItemsPerIter = 2;
+// One warp per item (row m, group of four 128-wide K blocks).  Lane l covers
+// elements [16 l, 16 l + 16) of the item's 512-element chunk, so lanes 8j..8j+7
+// own K block j.  The grid holds as many warps as are resident at once; each warp
+// walks a contiguous range of items two at a time and issues the loads of the
+// next pair before it quantizes the current one (four 16-byte loads in flight per
+// lane), so the stream never waits on a cold load between items.
+struct Item1x128 {
+  int m, qw, kb;
+  bool valid, active;
+};
 
-__device__ __forceinline__ void quant_item_1x128(const float (&f0)[8], const float (&f1)[8],
-                                                 bool active, int lane, int ue8m0, int m, int M,
-                                                 int qw, int kb, int nkb, int K, int ld,
+__device__ __forceinline__ Item1x128 item_1x128(int it, int end, int kq, int M, int nkb, int j) {
+  Item1x128 r;
+  r.valid = it < end;
+  r.m = it / kq;
+  r.qw = it - r.m * kq;
+  r.kb = 4 * r.qw + j;
+  r.active = r.valid && r.m < M && r.kb < nkb;
+  return r;
+}
+
+__device__ __forceinline__ void load_1x128(const __nv_bfloat16* __restrict__ X, const Item1x128& t,
+                                           int K, int lane, uint4 (&w)[2]) {
+  if (t.active) {
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<size_t>(t.m) * K +
+                                                      static_cast<size_t>(t.qw) * 512 + 16 * lane);
+    w[0] = __ldg(src);
+    w[1] = __ldg(src + 1);
+  }
+}
+
+__device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item1x128& t, int lane,
+                                                 int ue8m0, int M, int nkb, int K, int ld,
                                                  uint8_t* __restrict__ Xq, void* __restrict__ SF) {
+  float f0[8], f1[8];
   float amax = 0.0f;
-  if (active) {
+  if (t.active) {
+    unpack8(w[0], f0);
+    unpack8(w[1], f1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(f0[i]), fabsf(f1[i])));
   }
@@ -94,117 +121,110 @@ __device__ __forceinline__ void quant_item_1x128(const float (&f0)[8], const flo
   } else if (amax != 0.0f) {
     s = __fdiv_rn(amax, kE4M3Max);
   }
-  if (active) {
+  if (t.active) {
     const uint2 lo = quant8(f0, !ue8m0, s, inv), hi = quant8(f1, !ue8m0, s, inv);
-    *reinterpret_cast<uint4*>(Xq + static_cast<size_t>(m) * K + static_cast<size_t>(qw) * 512 +
+    *reinterpret_cast<uint4*>(Xq + static_cast<size_t>(t.m) * K + static_cast<size_t>(t.qw) * 512 +
                               16 * lane) = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
   if (ue8m0) {
     // gather the four exponent bytes of the group into one little-endian word
-    const uint32_t byte = active ? static_cast<uint32_t>(e + 127) : 0u;
+    const uint32_t byte = t.active ? static_cast<uint32_t>(e + 127) : 0u;
     const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
     const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
     const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
     if (lane == 0)
-      reinterpret_cast<uint32_t*>(SF)[static_cast<size_t>(qw) * ld + m] =
+      reinterpret_cast<uint32_t*>(SF)[static_cast<size_t>(t.qw) * ld + t.m] =
           byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-  } else if ((lane & 7) == 0 && kb < nkb) {
-    reinterpret_cast<float*>(SF)[static_cast<size_t>(kb) * ld + m] = (m < M) ? s : 0.0f;
+  } else if ((lane & 7) == 0 && t.kb < nkb) {
+    reinterpret_cast<float*>(SF)[static_cast<size_t>(t.kb) * ld + t.m] = (t.m < M) ? s : 0.0f;
   }
 }
 
 __global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16* __restrict__ X,
                                                              uint8_t* __restrict__ Xq,
                                                              void* __restrict__ SF, int M, int K,
-                                                             int ue8m0) {
+                                                             int ue8m0, int per_warp) {
   const int lane = threadIdx.x & 31;
   const int nkb = K / 128;
   const int kq = (nkb + 3) / 4;
   const int ld = (M + 3) / 4 * 4;
-  const long long items = static_cast<long long>(ld) * kq;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const int items = ld * kq;
   const int j = lane >> 3;                     // K block within the group
-  for (long long base = (static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) *
-                        kItemsPerIter;
-       base < items; base += warps * kItemsPerIter) {
-    int m[kItemsPerIter], qw[kItemsPerIter], kb[kItemsPerIter];
-    bool active[kItemsPerIter];
-    uint4 w[kItemsPerIter][2];
+  const int gw = static_cast<int>(blockIdx.x) * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
+  const long long first = static_cast<long long>(gw) * per_warp;
+  if (first >= items) return;                  // warp-uniform
+  int it = static_cast<int>(first);
+  const int end = min(it + per_warp, items);
+  uint4 cur[2][2], nxt[2][2];
+  Item1x128 tc[2], tn[2];
 #pragma unroll
-    for (int u = 0; u < kItemsPerIter; ++u) {
-      const long long it = base + u;
-      m[u] = static_cast<int>(it / kq);
-      qw[u] = static_cast<int>(it - static_cast<long long>(m[u]) * kq);
-      kb[u] = 4 * qw[u] + j;
-      active[u] = it < items && m[u] < M && kb[u] < nkb;
-      if (active[u]) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            X + static_cast<size_t>(m[u]) * K + static_cast<size_t>(qw[u]) * 512 + 16 * lane);
-        w[u][0] = __ldg(src);
-        w[u][1] = __ldg(src + 1);
-      }
+  for (int u = 0; u < 2; ++u) {
+    tc[u] = item_1x128(it + u, end, kq, M, nkb, j);
+    load_1x128(X, tc[u], K, lane, cur[u]);
+  }
+  for (; it < end; it += 2) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      tn[u] = item_1x128(it + 2 + u, end, kq, M, nkb, j);
+      load_1x128(X, tn[u], K, lane, nxt[u]);
     }
 #pragma unroll
-    for (int u = 0; u < kItemsPerIter; ++u) {
-      if (base + u >= items) break;             // warp-uniform
-      float f0[8], f1[8];
-      if (active[u]) {
-        unpack8(w[u][0], f0);
-        unpack8(w[u][1], f1);
-      }
-      quant_item_1x128(f0, f1, active[u], lane, ue8m0, m[u], M, qw[u], kb[u], nkb, K, ld, Xq, SF);
+    for (int u = 0; u < 2; ++u)
+      if (tc[u].valid) quant_item_1x128(cur[u], tc[u], lane, ue8m0, M, nkb, K, ld, Xq, SF);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      tc[u] = tn[u];
+      cur[u][0] = nxt[u][0];
+      cur[u][1] = nxt[u][1];
     }
   }
 }
 
-// One CTA per (expert g, 128-row block nb, group of four 128-wide K blocks), in
-// two passes over the 128 x 512 region so that every warp reads whole 1 KB row
-// segments: pass 1 finds each K block's max |w| (warp w takes rows w, w+8, ...,
-// lane l the 16 columns at 16 l, so lanes 8j..8j+7 cover K block j), pass 2
-// re-reads the region (an L2 hit: at most four such CTAs per SM keep the
-// working set well inside L2) and quantizes it with the block scales.
+// One CTA (256 threads) per (expert g, 128-row block nb, 128-wide K block kb), in
+// a single pass: the 32 KB block is loaded into registers (thread t holds the 8
+// columns at 8 (t % 16) of rows 16 i + t / 16, i = 0..7, so a half-warp reads one
+// 256-byte row segment), reduced to its max |w|, quantized from the registers and
+// written.  Weights are read from HBM exactly once.  UE8M0 exponents are written
+// as single bytes straight into their packed words (byte kb % 4 of the word of
+// each row), so the four CTAs sharing a word never read-modify-write it.
 __global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfloat16* __restrict__ W,
-                                                                  uint8_t* __restrict__ Wq,
-                                                                  void* __restrict__ SF, int N, int K,
-                                                                  int ue8m0) {
-  __shared__ float warp_max[8][4];
+                                                               uint8_t* __restrict__ Wq,
+                                                               void* __restrict__ SF, int N, int K,
+                                                               int ue8m0) {
+  __shared__ float warp_max[8];
   const int nkb = K / 128;
-  const int kq = (nkb + 3) / 4;
   const int nnb = (N + 127) / 128;
-  const int ldn = (N + 3) / 4 * 4;
-  const int qw = blockIdx.x % kq;
-  const int nb = (blockIdx.x / kq) % nnb;
-  const int g = blockIdx.x / (kq * nnb);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = lane >> 3;
-  const int kb = 4 * qw + j;
-  const bool col_ok = kb < nkb;
-  const size_t col = static_cast<size_t>(qw) * 512 + 16 * lane;
-  const __nv_bfloat16* Wg = W + static_cast<size_t>(g) * N * K;
-  uint8_t* Wqg = Wq + static_cast<size_t>(g) * N * K;
-  const int row0 = nb * 128 + warp;
+  const int kb = static_cast<int>(blockIdx.x % nkb);
+  const int nb = static_cast<int>((blockIdx.x / nkb) % nnb);
+  const int g = static_cast<int>(blockIdx.x / (static_cast<unsigned>(nkb) * nnb));
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int rsub = t >> 4;
+  const size_t col = static_cast<size_t>(kb) * 128 + 8 * (t & 15);
+  const __nv_bfloat16* Wg = W + static_cast<size_t>(g) * N * K + col;
+  uint8_t* Wqg = Wq + static_cast<size_t>(g) * N * K + col;
 
-  // pass 1: block maxima
-  float amax = 0.0f;
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int n = row0 + 8 * i;
-    if (col_ok && n < N) {
-      const uint4* src = reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(n) * K + col);
-      float f0[8], f1[8];
-      unpack8(__ldg(src), f0);
-      unpack8(__ldg(src + 1), f1);
+  uint4 w[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) amax = fmaxf(amax, fmaxf(fabsf(f0[x]), fabsf(f1[x])));
-    }
+  for (int i = 0; i < 8; ++i) {
+    const int n = nb * 128 + 16 * i + rsub;
+    w[i] = n < N ? __ldg(reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(n) * K))
+                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float f[8];
+    unpack8(w[i], f);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) amax = fmaxf(amax, fabsf(f[x]));
   }
 #pragma unroll
-  for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if ((lane & 7) == 0) warp_max[warp][j] = amax;
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (lane == 0) warp_max[warp] = amax;
   __syncthreads();
-  amax = warp_max[0][j];
+  amax = warp_max[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, warp_max[w][j]);
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
 
   float s = 1.0f, inv = 1.0f;
   int e = 0;
@@ -214,37 +234,30 @@ __global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfl
   } else if (amax != 0.0f) {
     s = __fdiv_rn(amax, kE4M3Max);
   }
-
-  // pass 2: quantize
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int n = row0 + 8 * i;
-    if (col_ok && n < N) {
-      const uint4* src = reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(n) * K + col);
-      float f0[8], f1[8];
-      unpack8(__ldg(src), f0);
-      unpack8(__ldg(src + 1), f1);
-      const uint2 lo = quant8(f0, !ue8m0, s, inv), hi = quant8(f1, !ue8m0, s, inv);
-      *reinterpret_cast<uint4*>(Wqg + static_cast<size_t>(n) * K + col) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = nb * 128 + 16 * i + rsub;
+    if (n < N) {
+      float f[8];
+      unpack8(w[i], f);
+      *reinterpret_cast<uint2*>(Wqg + static_cast<size_t>(n) * K) = quant8(f, !ue8m0, s, inv);
     }
   }
 
   // scale table
   if (!ue8m0) {
-    if (warp == 0 && (lane & 7) == 0 && col_ok)
-      reinterpret_cast<float*>(SF)[(static_cast<size_t>(g) * nnb + nb) * nkb + kb] = s;
-  } else {
-    const uint32_t byte = col_ok ? static_cast<uint32_t>(e + 127) : 0u;
-    const uint32_t b0 = __shfl_sync(0xffffffffu, byte, 0);
-    const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
-    const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
-    const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
-    const uint32_t word = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    if (threadIdx.x < 128) {
-      const int n = nb * 128 + threadIdx.x;
-      if (n < ldn)
-        reinterpret_cast<uint32_t*>(SF)[(static_cast<size_t>(g) * kq + qw) * ldn + n] =
-            (n < N) ? word : 0u;
+    if (t == 0) reinterpret_cast<float*>(SF)[(static_cast<size_t>(g) * nnb + nb) * nkb + kb] = s;
+  } else if (t < 128) {
+    const int kq = (nkb + 3) / 4;
+    const int ldn = (N + 3) / 4 * 4;
+    const int n = nb * 128 + t;
+    if (n < ldn) {
+      uint8_t* word = reinterpret_cast<uint8_t*>(SF) +
+                      ((static_cast<size_t>(g) * kq + kb / 4) * ldn + n) * 4;
+      word[kb & 3] = n < N ? static_cast<uint8_t>(e + 127) : static_cast<uint8_t>(0);
+      // the last K block also clears the bytes of the K blocks past the end
+      if (kb == nkb - 1)
+        for (int b = (kb & 3) + 1; b < 4; ++b) word[b] = 0;
     }
   }
 }
@@ -255,11 +268,22 @@ int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int f
                           cudaStream_t stream) {
   const int kq = (K / 128 + 3) / 4;
   const long long items = static_cast<long long>((M + 3) / 4 * 4) * kq;
-  const long long blocks_needed = (items + 8 * kItemsPerIter - 1) / (8 * kItemsPerIter);
-  const long long cap = static_cast<long long>(device_sm_count()) * 16;
-  const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
-  quantize_1x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(X),
-                                                  static_cast<uint8_t*>(Xq), SF, M, K, fmt);
+  if (items > 0x7F000000LL) return set_error(2, "quantize_1x128: problem too large");
+  static int blocks_per_sm = 0;
+  if (blocks_per_sm == 0) {
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_1x128_kernel, 256, 0);
+    if (e != cudaSuccess || b <= 0) return set_error(4, "quantize_1x128 occupancy: %s", cudaGetErrorString(e));
+    blocks_per_sm = b;
+  }
+  // one resident wave of warps, each with a contiguous range of items
+  const long long warps_cap = static_cast<long long>(device_sm_count()) * blocks_per_sm * 8;
+  const long long warps = items < warps_cap ? items : warps_cap;
+  const long long per_warp = (items + warps - 1) / warps;
+  const long long grid = (warps + 7) / 8;
+  quantize_1x128_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<uint8_t*>(Xq), SF, M, K, fmt,
+      static_cast<int>(per_warp));
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return set_error(4, "quantize_1x128 launch: %s", cudaGetErrorString(err));
   return 0;
@@ -267,8 +291,7 @@ int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int f
 
 int launch_quantize_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, int fmt,
                             cudaStream_t stream) {
-  const int kq = (K / 128 + 3) / 4;
-  const long long grid = static_cast<long long>(G) * ((N + 127) / 128) * kq;
+  const long long grid = static_cast<long long>(G) * ((N + 127) / 128) * (K / 128);
   if (grid > 0x7FFFFFFFLL) return set_error(2, "quantize_128x128: problem too large");
   quantize_128x128_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(W), static_cast<uint8_t*>(Wq), SF, N, K, fmt);
