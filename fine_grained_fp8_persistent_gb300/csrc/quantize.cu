@@ -55,12 +55,15 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   }
 }
 
-// Quantize 8 values with the group's scale; returns 8 packed E4M3 bytes.
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], bool f32_scale, float s,
-                                        float inv_pow2) {
+// Quantize 8 values with the group's scale; returns 8 packed E4M3 bytes.  FP32
+// scales divide (x / s, rounded to nearest); power-of-two scales multiply by the
+// exact 2^-e.  The format is a template parameter so each kernel carries only its
+// own arithmetic.
+template <bool UE8M0>
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float inv_pow2) {
   float q[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = f32_scale ? __fdiv_rn(f[i], s) : f[i] * inv_pow2;
+  for (int i = 0; i < 8; ++i) q[i] = UE8M0 ? f[i] * inv_pow2 : __fdiv_rn(f[i], s);
   uint2 r;
   r.x = static_cast<uint32_t>(ptx::cvt_e4m3x2(q[0], q[1])) |
         (static_cast<uint32_t>(ptx::cvt_e4m3x2(q[2], q[3])) << 16);
@@ -100,8 +103,9 @@ __device__ __forceinline__ void load_1x128(const __nv_bfloat16* __restrict__ X, 
   }
 }
 
+template <bool UE8M0>
 __device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item1x128& t, int lane,
-                                                 int ue8m0, int M, int nkb, int K, int ld,
+                                                 int M, int nkb, int K, int ld,
                                                  uint8_t* __restrict__ Xq, void* __restrict__ SF) {
   float f0[8], f1[8];
   float amax = 0.0f;
@@ -115,18 +119,18 @@ __device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item
   for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   float s = 1.0f, inv = 1.0f;
   int e = 0;
-  if (ue8m0) {
+  if (UE8M0) {
     e = ue8m0_exponent(amax);
     inv = exp2_neg(e);
   } else if (amax != 0.0f) {
     s = __fdiv_rn(amax, kE4M3Max);
   }
   if (t.active) {
-    const uint2 lo = quant8(f0, !ue8m0, s, inv), hi = quant8(f1, !ue8m0, s, inv);
+    const uint2 lo = quant8<UE8M0>(f0, s, inv), hi = quant8<UE8M0>(f1, s, inv);
     *reinterpret_cast<uint4*>(Xq + static_cast<size_t>(t.m) * K + static_cast<size_t>(t.qw) * 512 +
                               16 * lane) = make_uint4(lo.x, lo.y, hi.x, hi.y);
   }
-  if (ue8m0) {
+  if (UE8M0) {
     // gather the four exponent bytes of the group into one little-endian word
     const uint32_t byte = t.active ? static_cast<uint32_t>(e + 127) : 0u;
     const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
@@ -140,10 +144,11 @@ __device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item
   }
 }
 
+template <bool UE8M0>
 __global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16* __restrict__ X,
                                                              uint8_t* __restrict__ Xq,
                                                              void* __restrict__ SF, int M, int K,
-                                                             int ue8m0, int per_warp) {
+                                                             int per_warp) {
   const int lane = threadIdx.x & 31;
   const int nkb = K / 128;
   const int kq = (nkb + 3) / 4;
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u)
-      if (tc[u].valid) quant_item_1x128(cur[u], tc[u], lane, ue8m0, M, nkb, K, ld, Xq, SF);
+      if (tc[u].valid) quant_item_1x128<UE8M0>(cur[u], tc[u], lane, M, nkb, K, ld, Xq, SF);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       tc[u] = tn[u];
@@ -187,10 +192,10 @@ __global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16
 // written.  Weights are read from HBM exactly once.  UE8M0 exponents are written
 // as single bytes straight into their packed words (byte kb % 4 of the word of
 // each row), so the four CTAs sharing a word never read-modify-write it.
-__global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfloat16* __restrict__ W,
-                                                               uint8_t* __restrict__ Wq,
-                                                               void* __restrict__ SF, int N, int K,
-                                                               int ue8m0) {
+template <bool UE8M0>
+__global__ void __launch_bounds__(256, 3) quantize_128x128_kernel(const __nv_bfloat16* __restrict__ W,
+                                                                  uint8_t* __restrict__ Wq,
+                                                                  void* __restrict__ SF, int N, int K) {
   __shared__ float warp_max[8];
   const int nkb = K / 128;
   const int nnb = (N + 127) / 128;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfl
 
   float s = 1.0f, inv = 1.0f;
   int e = 0;
-  if (ue8m0) {
+  if (UE8M0) {
     e = ue8m0_exponent(amax);
     inv = exp2_neg(e);
   } else if (amax != 0.0f) {
@@ -240,12 +245,12 @@ __global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfl
     if (n < N) {
       float f[8];
       unpack8(w[i], f);
-      *reinterpret_cast<uint2*>(Wqg + static_cast<size_t>(n) * K) = quant8(f, !ue8m0, s, inv);
+      *reinterpret_cast<uint2*>(Wqg + static_cast<size_t>(n) * K) = quant8<UE8M0>(f, s, inv);
     }
   }
 
   // scale table
-  if (!ue8m0) {
+  if (!UE8M0) {
     if (t == 0) reinterpret_cast<float*>(SF)[(static_cast<size_t>(g) * nnb + nb) * nkb + kb] = s;
   } else if (t < 128) {
     const int kq = (nkb + 3) / 4;
@@ -264,15 +269,18 @@ __global__ void __launch_bounds__(256, 4) quantize_128x128_kernel(const __nv_bfl
 
 }  // namespace
 
-int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int fmt,
-                          cudaStream_t stream) {
+namespace {
+
+template <bool UE8M0>
+int launch_1x128(const void* X, void* Xq, void* SF, int M, int K, cudaStream_t stream) {
   const int kq = (K / 128 + 3) / 4;
   const long long items = static_cast<long long>((M + 3) / 4 * 4) * kq;
   if (items > 0x7F000000LL) return set_error(2, "quantize_1x128: problem too large");
   static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {
     int b = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_1x128_kernel, 256, 0);
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_1x128_kernel<UE8M0>, 256, 0);
     if (e != cudaSuccess || b <= 0) return set_error(4, "quantize_1x128 occupancy: %s", cudaGetErrorString(e));
     blocks_per_sm = b;
   }
@@ -281,24 +289,36 @@ int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int f
   const long long warps = items < warps_cap ? items : warps_cap;
   const long long per_warp = (items + warps - 1) / warps;
   const long long grid = (warps + 7) / 8;
-  quantize_1x128_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<uint8_t*>(Xq), SF, M, K, fmt,
-      static_cast<int>(per_warp));
+  quantize_1x128_kernel<UE8M0><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(X), static_cast<uint8_t*>(Xq), SF, M, K, static_cast<int>(per_warp));
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return set_error(4, "quantize_1x128 launch: %s", cudaGetErrorString(err));
   return 0;
 }
 
-int launch_quantize_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, int fmt,
-                            cudaStream_t stream) {
+template <bool UE8M0>
+int launch_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, cudaStream_t stream) {
   const long long grid = static_cast<long long>(G) * ((N + 127) / 128) * (K / 128);
   if (grid > 0x7FFFFFFFLL) return set_error(2, "quantize_128x128: problem too large");
-  quantize_128x128_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(W), static_cast<uint8_t*>(Wq), SF, N, K, fmt);
+  quantize_128x128_kernel<UE8M0><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(W), static_cast<uint8_t*>(Wq), SF, N, K);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess)
     return set_error(4, "quantize_128x128 launch: %s", cudaGetErrorString(err));
   return 0;
+}
+
+}  // namespace
+
+int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int fmt,
+                          cudaStream_t stream) {
+  return fmt ? launch_1x128<true>(X, Xq, SF, M, K, stream) : launch_1x128<false>(X, Xq, SF, M, K, stream);
+}
+
+int launch_quantize_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, int fmt,
+                            cudaStream_t stream) {
+  return fmt ? launch_128x128<true>(W, Wq, SF, G, N, K, stream)
+             : launch_128x128<false>(W, Wq, SF, G, N, K, stream);
 }
 
 }  // namespace fgf8
