@@ -345,11 +345,16 @@ def _e2e(args, fg, x_cpu, w_cpu, dev, stream) -> dict:
 
 
 def _variants(fg, dev, stream) -> dict:
-    """Kernel-only throughput of the other GEMM forms on their own workloads."""
+    """Kernel-only throughput of every other configuration on its own workload,
+    each against the roofline that bounds it: the dense FP8 (2 x bf16) or bf16
+    tensor peak for the large GEMMs, the HBM copy bandwidth for the skinny and
+    masked-decode GEMMs and the quantizers (algorithmic bytes: every operand,
+    scale table and output once; padding rows and empty experts excluded)."""
     import torch
     from fine_grained_fp8_persistent_gb300 import inputs
     out = {}
-    bf16_peak, _, _, src = _peaks()
+    bf16_peak, _, hbm, src = _peaks()
+    fp8_peak = 2.0 * bf16_peak
 
     def timeit(fn, iters=10):
         for _ in range(3):
@@ -368,34 +373,98 @@ def _variants(fg, dev, stream) -> dict:
             tot += es[2 * i].elapsed_time(es[2 * i + 1])
         return tot / iters
 
-    x = inputs.normal_bf16((M_TOK, K_IN), 1, outliers=True).to(dev)
+    def record(name, ms, flops, byts, bound):
+        r = {"ms": round(ms, 4), "bound": bound}
+        if flops:
+            r["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
+        r["GB/s"] = round(byts / (ms * 1e-3) / 1e9, 1)
+        if bound == "tensor_fp8":
+            r["frac"] = round(r["TFLOP/s"] / fp8_peak, 4)
+        elif bound == "tensor_bf16":
+            r["frac"] = round(r["TFLOP/s"] / bf16_peak, 4)
+        elif bound == "hbm":
+            r["frac"] = round(r["GB/s"] / hbm, 4)
+        r["tile"] = fg.last_tile() if flops else None
+        out[name] = r
+
+    def sf_bytes(rows, k, fmt):
+        return rows * (k // 128) * 4 if fmt == fg.SCALE_F32 else rows * ((k // 128 + 3) // 4) * 4
+
+    # FP8 block-scaled dense: the 128 x 128 x 256 case, the M = 64 decode and the
+    # M = 4096 case with FP32 scales
     w = inputs.normal_bf16((N_OUT, K_IN), 2, outliers=True).to(dev)
-    for name, fmt in (("fp8_f32scale_4096x7168x7168", fg.SCALE_F32), ("fp8_ue8m0_64x7168x7168", fg.SCALE_UE8M0)):
-        m = 64 if "64x" in name else M_TOK
+    x = inputs.normal_bf16((M_TOK, K_IN), 1, outliers=True).to(dev)
+    small_a = inputs.normal_bf16((128, 256), 0).to(dev)
+    small_b = inputs.normal_bf16((128, 256), 1).to(dev)
+    xq, sfa = fg.quantize_1x128(small_a, fg.SCALE_F32)
+    wq, sfb = fg.quantize_128x128(small_b, fg.SCALE_F32)
+    d = torch.empty((128, 128), dtype=torch.bfloat16, device=dev)
+    ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fg.SCALE_F32, out=d))
+    record("fp8_f32scale_128x128x256", ms, 2.0 * 128 * 128 * 256, 2 * 128 * 256 + 128 * 128 * 2, "latency")
+    for name, m, fmt in (("fp8_ue8m0_64x7168x7168", 64, fg.SCALE_UE8M0),
+                         ("fp8_f32scale_64x7168x7168", 64, fg.SCALE_F32),
+                         ("fp8_f32scale_4096x7168x7168", M_TOK, fg.SCALE_F32)):
         xq, sfa = fg.quantize_1x128(x[:m].contiguous(), fmt)
         wq, sfb = fg.quantize_128x128(w, fmt)
         d = torch.empty((m, N_OUT), dtype=torch.bfloat16, device=dev)
         ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fmt, out=d))
-        tf = 2.0 * m * N_OUT * K_IN / (ms * 1e-3) / 1e12
-        byts = m * K_IN + N_OUT * K_IN + m * N_OUT * 2
-        out[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                     "frac_fp8_peak": round(tf / (2 * bf16_peak), 4),
-                     "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+        byts = m * K_IN + N_OUT * K_IN + m * N_OUT * 2 + sf_bytes(m, K_IN, fmt) + sf_bytes(N_OUT, K_IN, fmt)
+        record(name, ms, 2.0 * m * N_OUT * K_IN, byts, "hbm" if m < 1024 else "tensor_fp8")
+    del x, xq, wq
+
+    # 16-bit dense 4096^3
     a = inputs.uniform_16bit((4096, 4096), 3).to(dev)
     b = inputs.uniform_16bit((4096, 4096), 4).to(dev)
     d16 = torch.empty((4096, 4096), dtype=torch.float16, device=dev)
     ms = timeit(lambda: fg.gemm_f16(a, b, out=d16))
-    tf = 2.0 * 4096 ** 3 / (ms * 1e-3) / 1e12
-    out["f16_4096x4096x4096"] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                                 "frac_bf16_peak": round(tf / bf16_peak, 4)}
+    record("f16_4096x4096x4096", ms, 2.0 * 4096 ** 3, 3 * 4096 * 4096 * 2, "tensor_bf16")
+    del a, b, d16
+
+    # grouped contiguous: 8 experts, N = 4096, K = 7168, counts multinomial(8192)
+    G, N, K = 8, 4096, 7168
+    counts = inputs.expert_counts(8192, G, 7)
+    m_idx, total = inputs.contiguous_layout(counts, fg.mk_alignment_for_contiguous())
+    ac = inputs.normal_bf16((total, K), 8, outliers=True).to(dev)
+    bc = inputs.normal_bf16((G, N, K), 9, outliers=True).to(dev)
+    m_idx = m_idx.to(dev)
+    valid = sum(counts)
+    for fmt, tag in ((fg.SCALE_UE8M0, "ue8m0"), (fg.SCALE_F32, "f32scale")):
+        aq, sfa = fg.quantize_1x128(ac, fmt)
+        bq, sfb = fg.quantize_128x128(bc, fmt)
+        dc = torch.empty((total, N), dtype=torch.bfloat16, device=dev)
+        ms = timeit(lambda: fg.grouped_fp8_contiguous(aq, sfa, bq, sfb, m_idx, fmt, out=dc))
+        byts = valid * K + G * N * K + valid * N * 2 + sf_bytes(valid, K, fmt) + G * sf_bytes(N, K, fmt)
+        record(f"grouped_contiguous_{tag}_8x4096x7168_m{valid}", ms, 2.0 * valid * N * K, byts, "tensor_fp8")
+    del ac, bc, aq, bq, dc
+
+    # grouped masked decode: 32 experts, Mmax = 256, N = 7168, K = 2048, FP32 scales
+    G, MM, N, K = 32, 256, 7168, 2048
+    mm = inputs.masked_rows(G, MM, 10)
+    am = inputs.normal_bf16((G, MM, K), 11, outliers=True).to(dev)
+    bm = inputs.normal_bf16((G, N, K), 12, outliers=True).to(dev)
+    fmt = fg.SCALE_F32
+    sh, dt = fg.sfa_shape(MM, K, fmt)
+    aq = torch.empty((G, MM, K), dtype=torch.uint8, device=dev)
+    sfa = torch.empty((G, *sh), dtype=dt, device=dev)
+    for g in range(G):
+        fg.quantize_1x128(am[g], fmt, aq[g], sfa[g])
+    bq, sfb = fg.quantize_128x128(bm, fmt)
+    mm_dev = mm.to(dev)
+    dm = torch.empty((G, MM, N), dtype=torch.bfloat16, device=dev)
+    ms = timeit(lambda: fg.grouped_fp8_masked(aq, sfa, bq, sfb, mm_dev, fmt, out=dm))
+    sm_ = int(mm.sum())
+    live = int((mm > 0).sum())
+    byts = sm_ * K + live * N * K + sm_ * N * 2 + sf_bytes(sm_, K, fmt) + live * sf_bytes(N, K, fmt)
+    record(f"grouped_masked_f32scale_32x256x7168x2048_m{sm_}", ms, 2.0 * sm_ * N * K, byts, "hbm")
+    del am, bm, aq, bq, dm
+
+    # quantizers (UE8M0)
     xb = inputs.normal_bf16((M_TOK, K_IN), 5, outliers=True).to(dev)
     ms = timeit(lambda: fg.quantize_1x128(xb, fg.SCALE_UE8M0))
-    byts = M_TOK * K_IN * 3 + M_TOK * K_IN // 128
-    out["quantize_1x128_4096x7168"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+    record("quantize_1x128_4096x7168", ms, 0, M_TOK * K_IN * 3 + sf_bytes(M_TOK, K_IN, 1), "hbm")
     wb = inputs.normal_bf16((N_OUT, K_IN), 6, outliers=True).to(dev)
     ms = timeit(lambda: fg.quantize_128x128(wb, fg.SCALE_UE8M0))
-    byts = N_OUT * K_IN * 3 + N_OUT * K_IN // 128
-    out["quantize_128x128_7168x7168"] = {"ms": round(ms, 4), "GB/s": round(byts / (ms * 1e-3) / 1e9, 1)}
+    record("quantize_128x128_7168x7168", ms, 0, N_OUT * K_IN * 3 + sf_bytes(N_OUT, K_IN, 1), "hbm")
     return out
 
 

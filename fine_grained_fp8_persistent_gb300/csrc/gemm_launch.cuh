@@ -17,11 +17,16 @@ struct TileCfg {
   double t_tile;  // relative time of one cluster tile (measured, see pick_cfg)
 };
 
-// Tiles of the problem for a configuration, counted per cluster (masked: upper
-// bound, every expert full).
+// Tiles of the problem for a configuration, counted per cluster (masked and
+// contiguous pairs: upper bounds).
 inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
   const long long tm = 128LL * c.ncta;
-  const long long mt = (a.M + tm - 1) / tm;
+  long long mt = (a.M + tm - 1) / tm;
+  if (s == Sched::Contiguous && c.ncta == 2) {
+    // pairs are cut per expert segment: each segment may end on half a pair
+    const long long blocks = (a.M + 127) / 128;
+    mt = (blocks + (a.G < blocks ? a.G : blocks) + 1) / 2;
+  }
   const long long nt = (a.N + c.bn - 1) / c.bn;
   const long long np = c.npair > 1 ? c.npair : 1;
   return (s == Sched::Masked ? a.G : 1) * mt * ((nt + np - 1) / np);
@@ -59,6 +64,10 @@ inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
   }
   return best;
 }
+
+// Contiguous layout on CTA pairs: the scheduler keeps one entry per expert
+// segment in shared memory, for at most this many 128-row blocks.
+constexpr int kMaxContiguousPairBlocks = 512;
 
 // Largest dynamic shared memory a CTA may opt into on sm_100-class parts (227 KB).
 constexpr int kMaxSmemOptin = 232448;

@@ -11,11 +11,9 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
   if constexpr (S == Sched::Dense) {
     if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 6, 2, 2>(a, tm, tiles, stream);
   }
-  if constexpr (S != Sched::Contiguous) {
-    if (c.ncta == 2) {
-      if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 6>(a, tm, tiles, stream);
-      return launch_persistent<Kind::MXF8, S, 2, 128, 8>(a, tm, tiles, stream);
-    }
+  if (c.ncta == 2) {
+    if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 6>(a, tm, tiles, stream);
+    return launch_persistent<Kind::MXF8, S, 2, 128, 8>(a, tm, tiles, stream);
   }
   switch (c.bn) {
     case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 4>(a, tm, tiles, stream);
@@ -29,16 +27,18 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
                      const void* Bq, const void* SFB, cudaStream_t stream) {
-  // the contiguous layout aligns expert segments to 128 rows: one CTA per tile
-  // relative tile times: see pick_cfg (the 64 and 32 widths are extrapolated)
+  // relative tile times: see pick_cfg (the 64 and 32 widths are extrapolated).
+  // The contiguous layout takes CTA pairs when its expert segments fit the
+  // scheduler's table (pairs are then cut per segment), else one CTA per tile.
   static const TileCfg dense_cands[] = {{2, 224, 2, 20.7}, {2, 224, 1, 18.4}, {2, 128, 1, 14.4},
                                         {1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
                                         {1, 32, 1, 6.3}};
   static const TileCfg pair_cands[] = {{2, 224, 1, 18.4}, {2, 128, 1, 14.4}, {1, 224, 1, 23.5},
                                        {1, 128, 1, 14.9}, {1, 64, 1, 9.1},   {1, 32, 1, 6.3}};
   static const TileCfg single_cands[] = {{1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1}, {1, 32, 1, 6.3}};
-  const TileCfg* cands = sched == Sched::Dense ? dense_cands : (sched == Sched::Masked ? pair_cands : single_cands);
-  const int n = sched == Sched::Dense ? 7 : (sched == Sched::Masked ? 6 : 4);
+  const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
+  const TileCfg* cands = sched == Sched::Dense ? dense_cands : (pairs ? pair_cands : single_cands);
+  const int n = sched == Sched::Dense ? 7 : (pairs ? 6 : 4);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;

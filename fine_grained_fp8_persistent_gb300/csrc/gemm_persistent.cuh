@@ -295,7 +295,14 @@ struct PCfg {
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
-  static constexpr int PREFIX_BYTES = (SCHED == Sched::Masked) ? (MAX_GROUPS + 1) * 4 : 0;
+  // contiguous layout on CTA pairs: tiles are cut per expert segment (run of
+  // 128-row blocks with the same expert), so the scheduler keeps each run's first
+  // block, expert and tile prefix; at most MAX_RUNS runs (M <= MAX_RUNS * 128)
+  static constexpr bool kRuns = SCHED == Sched::Contiguous && NCTA == 2;
+  static constexpr int MAX_RUNS = 512;
+  static constexpr int PREFIX_BYTES = (SCHED == Sched::Masked) ? (MAX_GROUPS + 1) * 4
+                                      : kRuns                  ? 3 * (MAX_RUNS + 1) * 4
+                                                               : 0;
   static constexpr int SMEM_BYTES = OFF_PREFIX + PREFIX_BYTES + 1024;
 
   static constexpr int ACC_COLS = NACC * BN;
@@ -433,6 +440,62 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       if (lane == 0) prefix[0] = 0;
     }
   }
+  // contiguous pairs: runs of 128-row blocks whose first row names the same expert
+  int* run_start = prefix + (C::MAX_RUNS + 1);          // first block of run r; [R] = nblk
+  int* run_expert = prefix + 2 * (C::MAX_RUNS + 1);
+  if constexpr (C::kRuns) {
+    if (warp == 2) {
+      const int nblk = M / C::BM;
+      int nrun = 0;
+      int prev = 0;
+      bool ok = nblk <= C::MAX_RUNS;
+      for (int b0 = 0; ok && b0 < nblk; b0 += 32) {
+        const int b = b0 + static_cast<int>(lane);
+        const int e = b < nblk ? __ldg(args.m_indices + static_cast<size_t>(b) * C::BM) : 0;
+        int up = __shfl_up_sync(0xffffffffu, e, 1);
+        if (lane == 0) up = prev;
+        const bool start = b < nblk && (b == 0 || e != up);
+        const uint32_t bal = __ballot_sync(0xffffffffu, start);
+        if (start) {
+          const int r = nrun + __popc(bal & ((1u << lane) - 1u));
+          run_start[r] = b;
+          run_expert[r] = e;
+        }
+        nrun += __popc(bal);
+        prev = __shfl_sync(0xffffffffu, e, 31);
+      }
+      if (!ok) {
+        if (lane == 0) atomicOr(args.status, FGF8_DEVERR_INPUT);
+        nrun = 0;
+      }
+      __syncwarp();
+      if (lane == 0) run_start[nrun] = nblk;
+      __syncwarp();
+      // pair tiles of run r: ceil(blocks / 2) x N tiles (runs of padding or of an
+      // out-of-range expert contribute none)
+      int acc = 0;
+      for (int r0 = 0; r0 < nrun; r0 += 32) {
+        const int r = r0 + static_cast<int>(lane);
+        int v = 0;
+        if (r < nrun) {
+          const int e = run_expert[r];
+          const int len = run_start[r + 1] - run_start[r];
+          v = (e >= 0 && e < G) ? (len + 1) / 2 * num_n : 0;
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, v, off);
+          if (static_cast<int>(lane) >= off) v += o;
+        }
+        if (r < nrun) prefix[r + 1] = acc + v;
+        acc += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) {
+        prefix[0] = 0;
+        run_expert[C::MAX_RUNS] = nrun;                 // the run count, for the schedulers
+      }
+    }
+  }
   if (warp == 1) {
     tc_alloc<NCTA>(ptx::smem_u32(tmem_slot), C::TMEM_ALLOC);
     ptx::tc_fence_before();
@@ -443,11 +506,39 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
   const uint32_t tmem_base = *tmem_slot;
 
   int num_tiles;
-  if constexpr (SCHED == Sched::Masked) num_tiles = prefix[G];
-  else num_tiles = num_m * num_nn;
+  int num_runs = 0;
+  if constexpr (SCHED == Sched::Masked) {
+    num_tiles = prefix[G];
+  } else if constexpr (C::kRuns) {
+    num_runs = run_expert[C::MAX_RUNS];
+    num_tiles = prefix[num_runs];
+  } else {
+    num_tiles = num_m * num_nn;
+  }
 
   auto get_tile = [&](int t, Tile& tl) -> bool {
     int m, n, g = 0, rows;
+    if constexpr (C::kRuns) {
+      int lo = 0, hi = num_runs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      const int len = run_start[lo + 1] - run_start[lo];
+      const int pt = (len + 1) / 2;                 // pair tiles of the run along M
+      const int local = t - prefix[lo];
+      n = local / pt;                               // pairs sharing a B tile are adjacent
+      const int j = local - n * pt;
+      const int half = 2 * j + static_cast<int>(rank);
+      g = run_expert[lo];
+      tl.a_row0 = (run_start[lo] + half) * C::BM;
+      tl.m_blk = tl.a_row0;                         // activation scales are indexed by global row
+      tl.n_blk = n;
+      tl.group = g;
+      tl.b_row0 = g * N + n * BN + static_cast<int>(rank) * C::BN_LOCAL;
+      tl.row_limit = half < len ? C::BM : 0;        // the half past the run's end stores nothing
+      return true;
+    }
     if constexpr (SCHED == Sched::Masked) {
       int lo = 0, hi = G - 1;
       while (lo < hi) {

@@ -82,6 +82,30 @@ def test_contiguous_full_size_sampled(fg, dev, oracle, fmt):
     assert bool(torch.isfinite(out[torch.from_numpy(valid_rows).to(dev)].float()).all())
 
 
+# Forced tile configurations of the contiguous layout.  CTA pairs are cut per
+# expert segment: segments of 3, 1, 0 and 2 blocks of 128 rows leave half pairs
+# whose second CTA stores nothing; N = 456 leaves a ragged last N tile and K = 640
+# an odd number of K blocks.
+CONTIG_TILES = [(1, "2x224"), (1, "2x128"), (1, "1x224"), (1, "1x128"), (0, "2x128"), (0, "1x256"),
+                (0, "1x128")]
+
+
+@pytest.mark.parametrize("fmt,tile", CONTIG_TILES)
+def test_contiguous_every_tile(fg, dev, oracle, monkeypatch, fmt, tile):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    case = _contig_case((300, 70, 0, 200), 456, 640, fmt, 21)
+    out = _run_contig(fg, dev, case, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    assert fg.last_tile() == f"{'mxf8' if fmt else 'f8f32'} contiguous {tile}"
+    m_idx, aq, sfa, bq, sfb = case
+    ref, _ = oracle.grouped_contiguous(aq, sfa, bq, sfb, m_idx, fmt)
+    o = out.float().cpu().numpy()
+    rows = m_idx >= 0
+    gemm_close(o[rows], ref[rows], f"contiguous {tile} fmt{fmt}")
+    assert np.isnan(o[~rows]).all(), "padding rows were written"
+
+
 def test_contiguous_bad_row_is_reported(fg, dev):
     case = _contig_case((128, 128), 128, 256, 0, 9)
     m_idx, aq, sfa, bq, sfb = case
