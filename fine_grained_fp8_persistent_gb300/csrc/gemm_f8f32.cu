@@ -9,7 +9,7 @@ template <Sched S>
 int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
                cudaStream_t stream) {
   // pairs: 128-wide tiles so that four partial buffers fit in TMEM
-  if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 9, 4>(a, tm, tiles, stream);
+  if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 8, 4>(a, tm, tiles, stream);
   switch (c.bn) {
     case 256: return launch_persistent<Kind::F8F32, S, 1, 256, 4>(a, tm, tiles, stream);
     case 128: return launch_persistent<Kind::F8F32, S, 1, 128, 6, 4>(a, tm, tiles, stream);
@@ -21,9 +21,9 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
                       cudaStream_t stream) {
-  // relative tile times: see pick_cfg (the 64 width is extrapolated)
-  static const TileCfg pair_cands[] = {{2, 128, 1, 23.4}, {1, 256, 1, 36.1}, {1, 128, 1, 23.6}, {1, 64, 1, 14.0}};
-  static const TileCfg single_cands[] = {{1, 256, 1, 36.1}, {1, 128, 1, 23.6}, {1, 64, 1, 14.0}};
+  // relative tile times: see pick_cfg
+  static const TileCfg pair_cands[] = {{2, 128, 1, 21.2}, {1, 256, 1, 33.0}, {1, 128, 1, 21.7}, {1, 64, 1, 19.3}};
+  static const TileCfg single_cands[] = {{1, 256, 1, 33.0}, {1, 128, 1, 21.7}, {1, 64, 1, 19.3}};
   // the contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment)
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;

@@ -255,9 +255,10 @@ struct PCfg {
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
   // K blocks per pipeline unit: one full/empty handshake, one hand-off to the MMA
-  // warp and one commit per unit.  The FP32-scale path hands every K block's
-  // partial product to the promotion warps, so its unit is one K block.
-  static constexpr int KPU = kF32S ? 1 : 2;
+  // warp and one stage-release commit per unit.  The FP32-scale path gives every
+  // K block of a unit its own partial buffer, so it takes two K blocks per unit
+  // only where four partial buffers fit (two units in flight).
+  static constexpr int KPU = kF32S ? (NACC_ >= 4 ? 2 : 1) : 2;
   static_assert(STAGES % KPU == 0, "stages per unit");
   static constexpr int UNITS = STAGES / KPU;
   static constexpr int SF_WARPS = kMX ? 4 : 0;
@@ -326,6 +327,13 @@ struct PCfg {
 // completed barrier, 43 from any other warp).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16]) {
+  ptx::tmem_ld_32x32b_x16(taddr, r);
+}
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32]) {
+  ptx::tmem_ld_32x32b_x32(taddr, r);
 }
 
 __device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
@@ -643,11 +651,13 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
             if constexpr (C::kMX) {
               if (kb0 % 4 == 0) sf_col = tmem_base + C::SF_COL0 + (gctr % C::SF_SLOTS) * C::SF_SLOT_COLS;
             }
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
 #pragma unroll
             for (int j = 0; j < C::KPU; ++j) {
               if (j < nk) {
                 const int kb = kb0 + j;
+                // FP32 scales: K block j of the unit has its own partial buffer
+                const int buf = C::kF32S ? (acc + j) % C::NACC : acc;
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
                 const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
                 const uint64_t bd = bdesc0 + stage * (C::B_BYTES >> 4);
@@ -660,17 +670,15 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
                   tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), id,
                                      sf_col, sf_col + 4, accum);
                 }
+                if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + buf), pair_mask);
               }
             }
             tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + unit), all_mask);
             if (group_end) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + gctr % C::SF_SLOTS), pair_mask);
-            if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
           }
           __syncwarp();
           if (group_end) ++gctr;
-          if constexpr (C::kF32S) {
-            if (++acc == C::NACC) acc = 0;
-          }
+          if constexpr (C::kF32S) acc = (acc + nk) % C::NACC;
           if (++unit == C::UNITS) unit = 0;
         }
         if constexpr (!C::kF32S) {
@@ -796,8 +804,13 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
           if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
         }
         for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
+          const int nk = min(C::KPU, nkb - kb0);
           if constexpr (C::kF32S) {
-            if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
+            // every partial buffer the unit writes has been drained by the promotion
+            for (int j = 0; j < nk; ++j) {
+              if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
+              if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+            }
           }
           if constexpr (C::kMX) {
             if (ok && kb0 % 4 == 0)
@@ -805,11 +818,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
           }
           if (ok) ok = pwait(bar(C::BAR_FULL + unit), phase, ctl);
           named_bar_sync(C::HANDOFF_BAR, 64);
-          const int kl = min(kb0 + C::KPU, nkb) - 1;
+          const int kl = kb0 + nk - 1;
           if (C::kMX && (kl % 4 == 3 || kl == nkb - 1)) ++gctr;
-          if constexpr (C::kF32S) {
-            if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
-          }
           if (++unit == C::UNITS) { unit = 0; phase ^= 1u; }
         }
         if constexpr (!C::kF32S) {
@@ -908,18 +918,34 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         if (!pwait(bar(C::BAR_ACC_FULL + pbuf), pphase, ctl)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pbuf * BN + h * HALF);
+        // chunks of CH columns, double-buffered: the load of chunk c + 1 is in
+        // flight while chunk c is accumulated; the buffer is released as soon as
+        // its last chunk has landed
+        constexpr int CH = HALF >= 128 ? 16 : 32;
+        constexpr int NCH = HALF / CH;
+        uint32_t va[CH], vb[CH];
+        tmem_ld_chunk(taddr, va);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(va);
 #pragma unroll
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
-          ptx::tmem_wait_ld();
-          if (c == HALF / 32 - 1) {
+        for (int c = 0; c < NCH; ++c) {
+          uint32_t(&cur)[CH] = (c & 1) ? vb : va;
+          uint32_t(&nxt)[CH] = (c & 1) ? va : vb;
+          if (c + 1 < NCH) {
+            tmem_ld_chunk(taddr + static_cast<uint32_t>(CH * (c + 1)), nxt);
+          } else {
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + pbuf));
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) accv[32 * c + j] = fmaf(s, __uint_as_float(v[j]), accv[32 * c + j]);
+          for (int j = 0; j < CH; j += 2)
+            ptx::ffma2(accv[CH * c + j], accv[CH * c + j + 1], s, __uint_as_float(cur[j]),
+                       __uint_as_float(cur[j + 1]));
+          if (c + 1 < NCH) {
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(nxt);
+          }
         }
         if (++pbuf == C::NACC) { pbuf = 0; pphase ^= 1u; }
       }

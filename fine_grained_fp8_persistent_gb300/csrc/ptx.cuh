@@ -158,6 +158,38 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr)
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Registers written by tcgen05.ld hold their values only after tcgen05.wait::ld.
+// Passing them through an empty volatile asm placed after the wait ties every
+// later use to the wait, so the compiler cannot hoist a use above it.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
+                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+// Two FP32 fused multiply-adds in one instruction: (a0, a1) += s * (x0, x1), each
+// lane rounded to nearest like fmaf.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x0, float x1) {
+  asm("{\n\t.reg .b64 xa, sa, ca;\n\t"
+      "mov.b64 xa, {%2, %3};\n\t"
+      "mov.b64 sa, {%4, %4};\n\t"
+      "mov.b64 ca, {%0, %1};\n\t"
+      "fma.rn.f32x2 ca, sa, xa, ca;\n\t"
+      "mov.b64 {%0, %1}, ca;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(s));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
