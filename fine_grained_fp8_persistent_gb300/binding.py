@@ -56,6 +56,7 @@ _SIGS = {
     "fgf8_last_error": ([], ctypes.c_char_p),
     "fgf8_last_tile": ([], ctypes.c_char_p),
     "fgf8_set_wait_timeout_ms": ([_I], _I),
+    "fgf8_selftest_wait_timeout": ([_P], _I),
     "fgf8_version": ([], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -233,6 +234,13 @@ def sfb_bytes(G: int, N: int, K: int, fmt) -> int:
 def last_tile() -> str:
     """Kernel configuration of the last GEMM this thread launched ("mxf8 dense 2x224")."""
     return (_lib.fgf8_last_tile() or b"").decode()
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Run the bounded-wait self-test: a wait on a barrier nothing signals, which
+    must give up after the current limit and leave FGF8_ERR_DEVICE_TIMEOUT (raw bits
+    0x801) for the next check_status()."""
+    _check(_lib.fgf8_selftest_wait_timeout(_stream(stream)), "fgf8_selftest_wait_timeout")
 
 
 def set_wait_timeout_ms(ms: int) -> int:

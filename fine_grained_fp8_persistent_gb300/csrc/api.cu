@@ -159,6 +159,14 @@ int fgf8_version(void) { return 100; }
 
 int fgf8_mk_alignment_for_contiguous(void) { return kBlockM; }
 
+int fgf8_selftest_wait_timeout(void* stream) {
+  int dev = 0;
+  if (int r = current_device(&dev)) return r;
+  uint32_t* status = fgf8::device_status_ptr();
+  if (status == nullptr) return FGF8_ERR_CUDA;
+  return fgf8::launch_wait_selftest(status, fgf8::wait_timeout_ns(), static_cast<cudaStream_t>(stream));
+}
+
 int fgf8_set_wait_timeout_ms(int ms) {
   const int prev = static_cast<int>(fgf8::wait_timeout_ns() / 1000000ull);
   if (ms > 0) g_timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;

@@ -12,6 +12,7 @@
 #define FGF8_DEVERR_ROLE_PRODUCER 0x100u
 #define FGF8_DEVERR_ROLE_MMA 0x200u
 #define FGF8_DEVERR_ROLE_EPILOGUE 0x400u
+#define FGF8_DEVERR_ROLE_SELFTEST 0x800u
 
 #ifndef __CUDACC_RTC__
 namespace fgf8 {
@@ -44,6 +45,8 @@ struct TensorMaps {
 
 // Host helpers (host.cu).
 int set_error(int code, const char* fmt, ...);
+// Launches the bounded-wait self-test (selftest.cu).
+int launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // Records the configuration of the GEMM launch this thread makes (fgf8_last_tile).
 void set_last_tile(const char* kind, const char* sched, int ctas, int bn);
 int device_sm_count();

@@ -687,14 +687,21 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
           if (++acc == C::NACC) acc = 0;
         }
       }
-      // every tcgen05 op issued completes before TMEM is released
+      // every tcgen05 op issued completes before TMEM is released; this wait
+      // ignores an earlier abort and gets at least a second, and if it still
+      // runs out the CTA takes the abort path, whose teardown grace period
+      // covers MMAs still in flight
       if (lane == 0) tc_commit<NCTA>(bar(C::BAR_DRAIN));
       __syncwarp();
       PairWaitCtl drain = ctl;
       uint32_t zero = 0;
       drain.abort_flag = &zero;
       drain.peer_abort = 0;
-      pwait(bar(C::BAR_DRAIN), 0u, drain);
+      drain.timeout_ns = ctl.timeout_ns > 1000000000ull ? ctl.timeout_ns : 1000000000ull;
+      if (!pwait(bar(C::BAR_DRAIN), 0u, drain)) {
+        aborted = true;
+        if (lane == 0) *abort_flag = 1u;
+      }
     }
   } else if (warp < 2 + C::SF_WARPS) {
     // ============================================================ scale-factor writers
@@ -859,6 +866,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
         ptx::tmem_wait_ld();
+        ptx::reg_fence(v);
         if (c == BN / 32 - 1) {
           ptx::tc_fence_before();
           __syncwarp();

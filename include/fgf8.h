@@ -169,7 +169,9 @@ FGF8_API long long fgf8_sfb_bytes(int G, int N, int K, int fmt);
  * fgf8_check_status -- synchronises `stream`, then reads and clears the status
  * word of the current device.  Returns FGF8_OK, FGF8_ERR_DEVICE_TIMEOUT,
  * FGF8_ERR_DEVICE_INPUT or FGF8_ERR_CUDA.  *raw_bits (if not NULL) receives the
- * raw word (bit 0 timeout, bit 1 input, bits 8-10 the role that timed out).
+ * raw word (bit 0 timeout, bit 1 input; bits 8-11 the role that timed out:
+ * 0x100 producer, 0x200 MMA issue / relay, 0x400 epilogue or promotion, 0x800
+ * the wait self-test).
  */
 FGF8_API int fgf8_check_status(void* stream, unsigned int* raw_bits);
 
@@ -181,6 +183,17 @@ FGF8_API const char* fgf8_last_error(void);
  * "" before the first launch.  The pointer stays valid until this thread's next
  * GEMM call. */
 FGF8_API const char* fgf8_last_tile(void);
+
+/*
+ * fgf8_selftest_wait_timeout -- diagnostic of the device-side failure path (no
+ * counterpart on the pages).  Launches one warp that waits, through the same
+ * bounded wait routine every GEMM role uses, on a barrier that nothing ever
+ * signals.  After the current wait limit (fgf8_set_wait_timeout_ms) the wait
+ * gives up and the kernel returns; the next fgf8_check_status() then reports
+ * FGF8_ERR_DEVICE_TIMEOUT with raw bits 0x801.  Nothing else is touched and the
+ * CUDA context stays usable.  Returns FGF8_OK once the kernel is enqueued.
+ */
+FGF8_API int fgf8_selftest_wait_timeout(void* stream);
 
 /* Upper bound, in milliseconds, on any single pipeline wait inside a kernel
  * (default 2000; also read from the environment variable FGF8_WAIT_TIMEOUT_MS
