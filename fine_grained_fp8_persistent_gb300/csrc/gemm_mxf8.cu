@@ -19,6 +19,7 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
     case 224: return launch_persistent<Kind::MXF8, S, 1, 224, 4>(a, tm, tiles, stream);
     case 128: return launch_persistent<Kind::MXF8, S, 1, 128, 6>(a, tm, tiles, stream);
     case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 8>(a, tm, tiles, stream);
+    case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 8>(a, tm, tiles, stream);
     default: return launch_persistent<Kind::MXF8, S, 1, 32, 8>(a, tm, tiles, stream);
   }
 }
@@ -27,18 +28,20 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
                      const void* Bq, const void* SFB, cudaStream_t stream) {
-  // relative tile times: see pick_cfg (the 64 and 32 widths are extrapolated).
+  // relative tile times: see pick_cfg (the 64, 48 and 32 widths are extrapolated).
   // The contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment), else one CTA per tile.
   static const TileCfg dense_cands[] = {{2, 224, 2, 20.7}, {2, 224, 1, 18.4}, {2, 128, 1, 14.4},
                                         {1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
-                                        {1, 32, 1, 6.3}};
+                                        {1, 48, 1, 8.0},   {1, 32, 1, 6.3}};
   static const TileCfg pair_cands[] = {{2, 224, 1, 18.4}, {2, 128, 1, 14.4}, {1, 224, 1, 23.5},
-                                       {1, 128, 1, 14.9}, {1, 64, 1, 9.1},   {1, 32, 1, 6.3}};
-  static const TileCfg single_cands[] = {{1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1}, {1, 32, 1, 6.3}};
+                                       {1, 128, 1, 14.9}, {1, 64, 1, 9.1},   {1, 48, 1, 8.0},
+                                       {1, 32, 1, 6.3}};
+  static const TileCfg single_cands[] = {{1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
+                                         {1, 48, 1, 8.0},   {1, 32, 1, 6.3}};
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
   const TileCfg* cands = sched == Sched::Dense ? dense_cands : (pairs ? pair_cands : single_cands);
-  const int n = sched == Sched::Dense ? 7 : (pairs ? 6 : 4);
+  const int n = sched == Sched::Dense ? 8 : (pairs ? 7 : 5);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;

@@ -242,7 +242,8 @@ struct PCfg {
   static constexpr int BN_LOCAL = BN / NCTA;        // B rows held by each CTA
   static constexpr int STAGES = STAGES_;
   static_assert(NCTA == 1 || NCTA == 2, "one CTA or a pair");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(KIND != Kind::F8F32 || BN % 64 == 0, "promotion halves of whole 32-column chunks");
   static_assert(BN_LOCAL % 16 == 0, "B rows per CTA");
   static constexpr bool kMX = KIND == Kind::MXF8;
   static constexpr bool kF32S = KIND == Kind::F8F32;
@@ -352,6 +353,24 @@ __device__ __forceinline__ void store_row32(void* D, size_t row_off, int col0, i
   uint16_t* out = reinterpret_cast<uint16_t*>(D) + row_off;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    const int col = col0 + 8 * j;
+    if (col < N) {
+      uint4 w;
+      w.x = pack_2x16(v[8 * j + 0], v[8 * j + 1], bf16);
+      w.y = pack_2x16(v[8 * j + 2], v[8 * j + 3], bf16);
+      w.z = pack_2x16(v[8 * j + 4], v[8 * j + 5], bf16);
+      w.w = pack_2x16(v[8 * j + 6], v[8 * j + 7], bf16);
+      *reinterpret_cast<uint4*>(out + col) = w;
+    }
+  }
+}
+
+// 16 consecutive FP32 values of one output row -> 16-bit, columns col0..col0+15.
+__device__ __forceinline__ void store_row16(void* D, size_t row_off, int col0, int N,
+                                            const float* v, bool bf16) {
+  uint16_t* out = reinterpret_cast<uint16_t*>(D) + row_off;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
     const int col = col0 + 8 * j;
     if (col < N) {
       uint4 w;
@@ -861,19 +880,34 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       }
       const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN);
+      // 32-column chunks, then a 16-column tail when BN is an odd multiple of 16;
+      // the accumulator is released after its last load
+      constexpr int NCH = BN / 32;
+      constexpr bool TAIL = (BN % 32) != 0;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
         ptx::tmem_wait_ld();
         ptx::reg_fence(v);
-        if (c == BN / 32 - 1) {
+        if (!TAIL && c == NCH - 1) {
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
         }
         if (row_ok)
           store_row32(args.D, row_off, tl.n_blk * BN + 32 * c, N, reinterpret_cast<const float*>(v), bf16);
+      }
+      if constexpr (TAIL) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(taddr + 32u * NCH, v);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(v);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
+        if (row_ok)
+          store_row16(args.D, row_off, tl.n_blk * BN + 32 * NCH, N, reinterpret_cast<const float*>(v), bf16);
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }

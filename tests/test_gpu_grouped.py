@@ -190,7 +190,7 @@ def test_masked_bad_count_is_reported(fg, dev):
     assert rc == 6 and bits & 2
 
 
-@pytest.mark.parametrize("tile", ["2x224", "2x128", "1x224", "1x64"])
+@pytest.mark.parametrize("tile", ["2x224", "2x128", "1x224", "1x64", "1x48"])
 def test_masked_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     masked = (0, 256, 17, 200)
