@@ -124,7 +124,7 @@ def test_host_validation_errors(fg, dev):
 # across the pair), or two pairs sharing A by TMA multicast.
 MXF8_TILES = ["4x224", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
 F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
-F16_TILES = ["4x256", "2x256", "1x128"]
+F16_TILES = ["4x256", "2x256", "2x224", "1x128"]
 
 
 @pytest.mark.parametrize("tile", MXF8_TILES)
