@@ -11,7 +11,7 @@ _EXPORTS = (
     "quantize_1x128", "quantize_128x128", "gemm_f16", "gemm_fp8_blockscaled",
     "grouped_fp8_contiguous", "grouped_fp8_masked", "check_status",
     "mk_alignment_for_contiguous", "sfa_bytes", "sfb_bytes", "sfa_shape", "sfb_shape",
-    "set_wait_timeout_ms", "selftest_wait_timeout", "last_error", "last_tile", "version", "FGF8Error", "SCALE_F32", "SCALE_UE8M0",
+    "set_wait_timeout_ms", "set_pdl", "selftest_wait_timeout", "last_error", "last_tile", "version", "FGF8Error", "SCALE_F32", "SCALE_UE8M0",
 )
 
 

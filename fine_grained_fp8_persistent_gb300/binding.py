@@ -57,6 +57,7 @@ _SIGS = {
     "fgf8_last_tile": ([], ctypes.c_char_p),
     "fgf8_set_wait_timeout_ms": ([_I], _I),
     "fgf8_selftest_wait_timeout": ([_P], _I),
+    "fgf8_set_pdl": ([_I], _I),
     "fgf8_version": ([], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -241,6 +242,11 @@ def selftest_wait_timeout(stream=None) -> None:
     must give up after the current limit and leave FGF8_ERR_DEVICE_TIMEOUT (raw bits
     0x801) for the next check_status()."""
     _check(_lib.fgf8_selftest_wait_timeout(_stream(stream)), "fgf8_selftest_wait_timeout")
+
+
+def set_pdl(enable: bool) -> bool:
+    """Turn programmatic dependent launch on or off; returns the previous setting."""
+    return bool(_lib.fgf8_set_pdl(1 if enable else 0))
 
 
 def set_wait_timeout_ms(ms: int) -> int:

@@ -21,6 +21,7 @@ constexpr int kMaxGroups = 1024; // masked scheduler keeps a per-expert prefix i
 __device__ uint32_t g_status;
 
 thread_local char g_errbuf[512];
+int g_pdl = -1;   // -1 = not read from the environment yet
 thread_local char g_last_tile[64];
 
 struct DevInfo {
@@ -75,6 +76,14 @@ namespace fgf8 {
 
 void set_last_tile(const char* kind, const char* sched, int ctas, int bn) {
   std::snprintf(g_last_tile, sizeof(g_last_tile), "%s %s %dx%d", kind, sched, ctas, bn);
+}
+
+bool pdl_enabled() {
+  if (g_pdl < 0) {
+    const char* e = std::getenv("FGF8_PDL");
+    g_pdl = (e != nullptr && e[0] == '0') ? 0 : 1;
+  }
+  return g_pdl != 0;
 }
 
 int set_error(int code, const char* fmt, ...) {
@@ -165,6 +174,12 @@ int fgf8_selftest_wait_timeout(void* stream) {
   uint32_t* status = fgf8::device_status_ptr();
   if (status == nullptr) return FGF8_ERR_CUDA;
   return fgf8::launch_wait_selftest(status, fgf8::wait_timeout_ns(), static_cast<cudaStream_t>(stream));
+}
+
+int fgf8_set_pdl(int enable) {
+  const int prev = fgf8::pdl_enabled() ? 1 : 0;
+  if (enable == 0 || enable == 1) g_pdl = enable;
+  return prev;
 }
 
 int fgf8_set_wait_timeout_ms(int ms) {

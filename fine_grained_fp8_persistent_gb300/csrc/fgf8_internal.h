@@ -45,6 +45,8 @@ struct TensorMaps {
 
 // Host helpers (host.cu).
 int set_error(int code, const char* fmt, ...);
+// Whether kernels are launched with programmatic stream serialization (PDL).
+bool pdl_enabled();
 // Launches the bounded-wait self-test (selftest.cu).
 int launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // Records the configuration of the GEMM launch this thread makes (fgf8_last_tile).

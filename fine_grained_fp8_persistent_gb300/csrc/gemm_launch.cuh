@@ -86,11 +86,13 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
     return set_error(2, "tile needs %d bytes of shared memory", C::SMEM_BYTES);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
@@ -113,6 +115,7 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
   long long clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   set_last_tile(KIND == Kind::F16 ? "f16" : KIND == Kind::MXF8 ? "mxf8" : "f8f32",
                 SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, a);

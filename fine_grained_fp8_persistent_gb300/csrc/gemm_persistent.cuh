@@ -445,6 +445,16 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
+  if (warp == 1) {
+    tc_alloc<NCTA>(ptx::smem_u32(tmem_slot), C::TMEM_ALLOC);
+    ptx::tc_fence_before();
+  }
+  // Everything above touches only this CTA's shared memory and TMEM, so under a
+  // programmatic dependent launch it overlaps the tail of the previous kernel.
+  // Every read of global data (operands, scales, m_indices, masked_m) comes after
+  // this wait.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   if constexpr (SCHED == Sched::Masked) {
     if (warp == 2) {
       int run = 0;
@@ -522,10 +532,6 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         run_expert[C::MAX_RUNS] = nrun;                 // the run count, for the schedulers
       }
     }
-  }
-  if (warp == 1) {
-    tc_alloc<NCTA>(ptx::smem_u32(tmem_slot), C::TMEM_ALLOC);
-    ptx::tc_fence_before();
   }
   __syncthreads();
   if constexpr (C::CLUSTER > 1) cluster_sync_all();   // peer barriers initialised before any remote use

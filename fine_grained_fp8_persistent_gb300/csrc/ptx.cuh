@@ -190,6 +190,16 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float s, float x0, f
       : "+f"(a0), "+f"(a1)
       : "f"(x0), "f"(x1), "f"(s));
 }
+// Programmatic dependent launch.  griddep_wait blocks until the grids this one
+// depends on have completed and their memory is visible (it returns at once when
+// the launch carried no programmatic dependency); griddep_launch_dependents lets
+// the next grid on the stream start its own set-up once every CTA of this grid
+// has issued it or exited (that grid still waits for this one to finish before it
+// reads anything).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

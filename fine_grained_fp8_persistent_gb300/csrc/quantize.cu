@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "fgf8_internal.h"
 #include "ptx.cuh"
@@ -149,6 +150,8 @@ __global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ Xq,
                                                              void* __restrict__ SF, int M, int K,
                                                              int per_warp) {
+  ptx::griddep_wait();                          // X may come from the previous kernel
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nkb = K / 128;
   const int kq = (nkb + 3) / 4;
@@ -197,6 +200,8 @@ __global__ void __launch_bounds__(256, 3) quantize_128x128_kernel(const __nv_bfl
                                                                   uint8_t* __restrict__ Wq,
                                                                   void* __restrict__ SF, int N, int K) {
   __shared__ float warp_max[8];
+  ptx::griddep_wait();                          // W may come from the previous kernel
+  ptx::griddep_launch_dependents();
   const int nkb = K / 128;
   const int nnb = (N + 127) / 128;
   const int kb = static_cast<int>(blockIdx.x % nkb);
@@ -271,6 +276,22 @@ __global__ void __launch_bounds__(256, 3) quantize_128x128_kernel(const __nv_bfl
 
 namespace {
 
+// 256-thread launch, with programmatic stream serialization when enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <bool UE8M0>
 int launch_1x128(const void* X, void* Xq, void* SF, int M, int K, cudaStream_t stream) {
   const int kq = (K / 128 + 3) / 4;
@@ -289,9 +310,9 @@ int launch_1x128(const void* X, void* Xq, void* SF, int M, int K, cudaStream_t s
   const long long warps = items < warps_cap ? items : warps_cap;
   const long long per_warp = (items + warps - 1) / warps;
   const long long grid = (warps + 7) / 8;
-  quantize_1x128_kernel<UE8M0><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(X), static_cast<uint8_t*>(Xq), SF, M, K, static_cast<int>(per_warp));
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err =
+      launch_pdl(quantize_1x128_kernel<UE8M0>, static_cast<unsigned>(grid), stream,
+                 static_cast<const __nv_bfloat16*>(X), static_cast<uint8_t*>(Xq), SF, M, K, static_cast<int>(per_warp));
   if (err != cudaSuccess) return set_error(4, "quantize_1x128 launch: %s", cudaGetErrorString(err));
   return 0;
 }
@@ -300,9 +321,8 @@ template <bool UE8M0>
 int launch_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, cudaStream_t stream) {
   const long long grid = static_cast<long long>(G) * ((N + 127) / 128) * (K / 128);
   if (grid > 0x7FFFFFFFLL) return set_error(2, "quantize_128x128: problem too large");
-  quantize_128x128_kernel<UE8M0><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(W), static_cast<uint8_t*>(Wq), SF, N, K);
-  const cudaError_t err = cudaGetLastError();
+  const cudaError_t err = launch_pdl(quantize_128x128_kernel<UE8M0>, static_cast<unsigned>(grid), stream,
+                                     static_cast<const __nv_bfloat16*>(W), static_cast<uint8_t*>(Wq), SF, N, K);
   if (err != cudaSuccess)
     return set_error(4, "quantize_128x128 launch: %s", cudaGetErrorString(err));
   return 0;

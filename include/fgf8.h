@@ -195,6 +195,14 @@ FGF8_API const char* fgf8_last_tile(void);
  */
 FGF8_API int fgf8_selftest_wait_timeout(void* stream);
 
+/* Programmatic dependent launch (on by default; the environment variable
+ * FGF8_PDL=0 turns it off at first use).  When on, every kernel is launched with
+ * programmatic stream serialization: its set-up (barriers, TMEM, descriptor
+ * prefetch) overlaps the end of the previous kernel on the stream, and it reads no
+ * global data before that kernel has completed.  enable: 1 on, 0 off, anything
+ * else leaves it unchanged.  Returns the previous setting. */
+FGF8_API int fgf8_set_pdl(int enable);
+
 /* Upper bound, in milliseconds, on any single pipeline wait inside a kernel
  * (default 2000; also read from the environment variable FGF8_WAIT_TIMEOUT_MS
  * at first use).  Returns the previous value. */
