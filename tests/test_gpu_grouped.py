@@ -218,3 +218,41 @@ def test_masked_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile):
     v = valid.astype(bool)
     gemm_close(o[v], ref[v], f"masked f32 {tile}")
     assert np.isnan(o[~v]).all()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_masked_maximum_expert_count(fg, dev, oracle, fmt):
+    """G = 1024 experts, the largest the masked scheduler's per-expert table holds."""
+    G, Mmax, N, K = 1024, 32, 128, 128
+    masked = inputs.masked_rows(G, Mmax, seed=11).numpy()
+    case = _masked_case(G, Mmax, N, K, fmt, 12)
+    out = _run_masked(fg, dev, case, masked, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ref, valid = oracle.grouped_masked(*case, masked, fmt)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    gemm_close(o[v], ref[v], "masked G=1024")
+    assert np.isnan(o[~v]).all()
+
+
+@pytest.mark.parametrize("counts,pairs", [((20000, 16000, 30000, 510), False),   # 521 blocks of 128 rows
+                                          ((16384, 16384, 16384, 16384), True)])  # exactly 512
+def test_contiguous_pair_table_limit(fg, dev, oracle, monkeypatch, counts, pairs):
+    """A CTA-pair tile is asked for.  Beyond the pair scheduler's segment table
+    (512 blocks of 128 rows) the launcher does not offer pairs and falls back to
+    one-CTA tiles; at the limit it still runs the pair."""
+    monkeypatch.setenv("FGF8_FORCE_TILE", "2x128")
+    fmt = 1
+    case = _contig_case(counts, 64, 128, fmt, 13)
+    out = _run_contig(fg, dev, case, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ctas = int(fg.last_tile().split()[-1].split("x")[0])
+    assert (ctas == 2) == pairs, fg.last_tile()
+    m_idx, aq, sfa, bq, sfb = case
+    ref, _ = oracle.grouped_contiguous(aq, sfa, bq, sfb, m_idx, fmt)
+    o = out.float().cpu().numpy()
+    rows = m_idx >= 0
+    gemm_close(o[rows], ref[rows], f"contiguous {sum(counts)} rows")
+    assert np.isnan(o[~rows]).all()
