@@ -284,7 +284,7 @@ def run_ours(args) -> None:
     value = _job_tflops(args.steps, world, t_max_ms)
 
     e2e = None if args.no_e2e else _e2e(args, fg, x_cpu, w_cpu, dev, stream, side, d)
-    variants = _variants(fg, dev, stream) if rank == 0 and not args.no_variants else None
+    variants = _variants(fg, dev, stream, args.variant) if rank == 0 and not args.no_variants else None
     cpu = _cpu_baseline(args) if rank == 0 and world == 1 and not args.no_cpu else None
 
     bf16_peak, bf16_sust, hbm, src = _peaks()
@@ -424,7 +424,7 @@ def _e2e(args, fg, x_cpu, w_cpu, dev, stream, side, d_device) -> dict:
             "result_matches_device_step": same}
 
 
-def _variants(fg, dev, stream) -> dict:
+def _variants(fg, dev, stream, only=None) -> dict:
     """Kernel-only throughput of every other configuration on its own workload,
     each against the roofline that bounds it: the dense FP8 (2 x bf16) or bf16
     tensor peak for the large GEMMs, the HBM copy bandwidth for the skinny and
@@ -467,6 +467,9 @@ def _variants(fg, dev, stream) -> dict:
         r["tile"] = fg.last_tile() if flops else None
         out[name] = r
 
+    def want(name):
+        return only is None or name.startswith(only)
+
     def sf_bytes(rows, k, fmt):
         return rows * (k // 128) * 4 if fmt == fg.SCALE_F32 else rows * ((k // 128 + 3) // 4) * 4
 
@@ -479,11 +482,14 @@ def _variants(fg, dev, stream) -> dict:
     xq, sfa = fg.quantize_1x128(small_a, fg.SCALE_F32)
     wq, sfb = fg.quantize_128x128(small_b, fg.SCALE_F32)
     d = torch.empty((128, 128), dtype=torch.bfloat16, device=dev)
-    ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fg.SCALE_F32, out=d))
-    record("fp8_f32scale_128x128x256", ms, 2.0 * 128 * 128 * 256, 2 * 128 * 256 + 128 * 128 * 2, "latency")
+    if want("fp8_f32scale_128x128x256"):
+        ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fg.SCALE_F32, out=d))
+        record("fp8_f32scale_128x128x256", ms, 2.0 * 128 * 128 * 256, 2 * 128 * 256 + 128 * 128 * 2, "latency")
     for name, m, fmt in (("fp8_ue8m0_64x7168x7168", 64, fg.SCALE_UE8M0),
                          ("fp8_f32scale_64x7168x7168", 64, fg.SCALE_F32),
                          ("fp8_f32scale_4096x7168x7168", M_TOK, fg.SCALE_F32)):
+        if not want(name):
+            continue
         xq, sfa = fg.quantize_1x128(x[:m].contiguous(), fmt)
         wq, sfb = fg.quantize_128x128(w, fmt)
         d = torch.empty((m, N_OUT), dtype=torch.bfloat16, device=dev)
@@ -493,14 +499,17 @@ def _variants(fg, dev, stream) -> dict:
     del x, xq, wq
 
     # 16-bit dense 4096^3
-    a = inputs.uniform_16bit((4096, 4096), 3).to(dev)
-    b = inputs.uniform_16bit((4096, 4096), 4).to(dev)
-    d16 = torch.empty((4096, 4096), dtype=torch.float16, device=dev)
-    ms = timeit(lambda: fg.gemm_f16(a, b, out=d16))
-    record("f16_4096x4096x4096", ms, 2.0 * 4096 ** 3, 3 * 4096 * 4096 * 2, "tensor_bf16")
-    del a, b, d16
+    if want("f16_4096x4096x4096"):
+        a = inputs.uniform_16bit((4096, 4096), 3).to(dev)
+        b = inputs.uniform_16bit((4096, 4096), 4).to(dev)
+        d16 = torch.empty((4096, 4096), dtype=torch.float16, device=dev)
+        ms = timeit(lambda: fg.gemm_f16(a, b, out=d16))
+        record("f16_4096x4096x4096", ms, 2.0 * 4096 ** 3, 3 * 4096 * 4096 * 2, "tensor_bf16")
+        del a, b, d16
 
     # grouped contiguous: 8 experts, N = 4096, K = 7168, counts multinomial(8192)
+    if not want("grouped_contiguous"):
+        return _variants_tail(fg, dev, timeit, record, sf_bytes, want, out)
     G, N, K = 8, 4096, 7168
     counts = inputs.expert_counts(8192, G, 7)
     m_idx, total = inputs.contiguous_layout(counts, fg.mk_alignment_for_contiguous())
@@ -516,8 +525,16 @@ def _variants(fg, dev, stream) -> dict:
         byts = valid * K + G * N * K + valid * N * 2 + sf_bytes(valid, K, fmt) + G * sf_bytes(N, K, fmt)
         record(f"grouped_contiguous_{tag}_8x4096x7168_m{valid}", ms, 2.0 * valid * N * K, byts, "tensor_fp8")
     del ac, bc, aq, bq, dc
+    return _variants_tail(fg, dev, timeit, record, sf_bytes, want, out)
 
+
+def _variants_tail(fg, dev, timeit, record, sf_bytes, want, out) -> dict:
+    """The masked-decode and quantizer variants (see _variants)."""
+    import torch
+    from fine_grained_fp8_persistent_gb300 import inputs
     # grouped masked decode: 32 experts, Mmax = 256, N = 7168, K = 2048, FP32 scales
+    if not want("grouped_masked"):
+        return _quantizer_variants(fg, dev, timeit, record, sf_bytes, want, out)
     G, MM, N, K = 32, 256, 7168, 2048
     mm = inputs.masked_rows(G, MM, 10)
     am = inputs.normal_bf16((G, MM, K), 11, outliers=True).to(dev)
@@ -537,14 +554,20 @@ def _variants(fg, dev, stream) -> dict:
     byts = sm_ * K + live * N * K + sm_ * N * 2 + sf_bytes(sm_, K, fmt) + live * sf_bytes(N, K, fmt)
     record(f"grouped_masked_f32scale_32x256x7168x2048_m{sm_}", ms, 2.0 * sm_ * N * K, byts, "hbm")
     del am, bm, aq, bq, dm
+    return _quantizer_variants(fg, dev, timeit, record, sf_bytes, want, out)
 
-    # quantizers (UE8M0)
-    xb = inputs.normal_bf16((M_TOK, K_IN), 5, outliers=True).to(dev)
-    ms = timeit(lambda: fg.quantize_1x128(xb, fg.SCALE_UE8M0))
-    record("quantize_1x128_4096x7168", ms, 0, M_TOK * K_IN * 3 + sf_bytes(M_TOK, K_IN, 1), "hbm")
-    wb = inputs.normal_bf16((N_OUT, K_IN), 6, outliers=True).to(dev)
-    ms = timeit(lambda: fg.quantize_128x128(wb, fg.SCALE_UE8M0))
-    record("quantize_128x128_7168x7168", ms, 0, N_OUT * K_IN * 3 + sf_bytes(N_OUT, K_IN, 1), "hbm")
+
+def _quantizer_variants(fg, dev, timeit, record, sf_bytes, want, out) -> dict:
+    """The two quantizers on the bench shapes (UE8M0)."""
+    from fine_grained_fp8_persistent_gb300 import inputs
+    if want("quantize_1x128_4096x7168"):
+        xb = inputs.normal_bf16((M_TOK, K_IN), 5, outliers=True).to(dev)
+        ms = timeit(lambda: fg.quantize_1x128(xb, fg.SCALE_UE8M0))
+        record("quantize_1x128_4096x7168", ms, 0, M_TOK * K_IN * 3 + sf_bytes(M_TOK, K_IN, 1), "hbm")
+    if want("quantize_128x128_7168x7168"):
+        wb = inputs.normal_bf16((N_OUT, K_IN), 6, outliers=True).to(dev)
+        ms = timeit(lambda: fg.quantize_128x128(wb, fg.SCALE_UE8M0))
+        record("quantize_128x128_7168x7168", ms, 0, N_OUT * K_IN * 3 + sf_bytes(N_OUT, K_IN, 1), "hbm")
     return out
 
 
@@ -635,6 +658,7 @@ def main() -> None:
     ap.add_argument("--ref-seconds", type=float, default=120.0, help="target length of an --impl reference run")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-variants", action="store_true", help="skip the extra kernel lines")
+    ap.add_argument("--variant", default=None, help="run only the variants whose name starts with this")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     if args.warmup < 3:
