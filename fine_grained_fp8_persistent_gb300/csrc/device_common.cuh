@@ -49,52 +49,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(2u) << 61;             // SWIZZLE_128B
   return d;
 }
-// Interleaved (no swizzle) K-major layout of 8-row x 16-byte core matrices stored
-// back to back: the 32 x 128-bit scale-factor tiles copied by tcgen05.cp.
-__device__ __forceinline__ uint64_t smem_desc_plain_rows16(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(0u) << 16;             // LBO: one core matrix along K
-  d |= static_cast<uint64_t>(128u >> 4) << 32;      // SBO: next 8 rows 128 B later
-  d |= static_cast<uint64_t>(1u) << 46;             // version
-  return d;                                         // layout type 0: no swizzle
-}
-
-// ---------------------------------------------------------------------------
-// Bounded waits.  Every wait on a barrier gives up after `timeout_ns`, raises the
-// CTA-wide abort flag and ORs an error bit into the device status word, so a
-// broken handshake ends the kernel instead of hanging the GPU.
-// ---------------------------------------------------------------------------
-struct WaitCtl {
-  volatile uint32_t* abort_flag;   // in shared memory
-  uint32_t* status;                // device status word (global)
-  uint64_t timeout_ns;
-  uint32_t role_bit;
-};
-
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*c.abort_flag) return false;
-      if (ptx::globaltimer() - t0 > c.timeout_ns) {
-        *c.abort_flag = 1u;
-        atomicOr(c.status, FGF8_DEVERR_TIMEOUT | c.role_bit);
-        return false;
-      }
-    }
-  }
-}
-
-// Warp-uniform form: every lane of the warp waits, and the warp agrees on the
-// outcome, so a warp never splits before a .sync.aligned instruction.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  const bool ok = wait_bar(bar, parity, c);
-  return __all_sync(0xffffffffu, ok) != 0;
-}
-
 // ---------------------------------------------------------------------------
 // Persistent tile schedulers.  A CTA walks tiles blockIdx.x, blockIdx.x+grid, ...
 // (the static round-robin of the DeepGEMM page's scheduler section); every role

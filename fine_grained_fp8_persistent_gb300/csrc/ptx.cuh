@@ -3,8 +3,8 @@
 // Sources for the instruction forms: "GPU GEMM part 4: tcgen05 & Blackwell"
 // (sections 2.3 TMEM allocation, 3.1 tcgen05.mma form, 3.6 commit/fence,
 // 4.1-4.2 tcgen05.ld shapes and constraints, 6.2 block_scale operands) and
-// "Blackwell Tensor Core: tcgen05.mma" (mlc.ai; SFA/SFB staged through SMEM and
-// tcgen05.cp into TMEM).
+// "Blackwell Tensor Core: tcgen05.mma" (mlc.ai; the scale operands of the
+// block-scaled MMA live in TMEM).
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -14,12 +14,6 @@ namespace ptx {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -55,10 +49,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// ----------------------------------------------------------------- fences
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -134,12 +124,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
-}
-// Copy a 32-row x 128-bit matrix from shared memory into TMEM, replicated into
-// the four 32-lane quarters (each warp quarter of the tensor core reads its own).
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05: TMEM loads

@@ -256,3 +256,30 @@ def test_contiguous_pair_table_limit(fg, dev, oracle, monkeypatch, counts, pairs
     rows = m_idx >= 0
     gemm_close(o[rows], ref[rows], f"contiguous {sum(counts)} rows")
     assert np.isnan(o[~rows]).all()
+
+
+def test_masked_in_a_cuda_graph(fg, dev, oracle):
+    """The masked layout reads its row counts on the device, so one captured call
+    serves any counts: capture once, change masked_m in place, replay."""
+    G, Mmax, N, K, fmt = 4, 256, 256, 384, 1
+    case = _masked_case(G, Mmax, N, K, fmt, 14)
+    aq, sfa, bq, sfb = (to_dev(a, dev) for a in case)
+    counts = torch.zeros(G, dtype=torch.int32, device=dev)
+    out = torch.empty((G, Mmax, N), dtype=torch.bfloat16, device=dev)
+    fg.grouped_fp8_masked(aq, sfa, bq, sfb, counts, fmt, out=out)      # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fg.grouped_fp8_masked(aq, sfa, bq, sfb, counts, fmt, out=out)
+    for masked in [(0, 256, 17, 1), (128, 0, 255, 64)]:
+        out.fill_(float("nan"))
+        counts.copy_(torch.tensor(masked, dtype=torch.int32))
+        graph.replay()
+        torch.cuda.synchronize()
+        rc, bits = fg.check_status()
+        assert rc == 0, hex(bits)
+        ref, valid = oracle.grouped_masked(*case, np.asarray(masked, np.int32), fmt)
+        o = out.float().cpu().numpy()
+        v = valid.astype(bool)
+        gemm_close(o[v], ref[v], f"graph replay {masked}")
+        assert np.isnan(o[~v]).all()
