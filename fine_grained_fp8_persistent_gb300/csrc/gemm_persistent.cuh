@@ -57,6 +57,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <type_traits>
 
 #include "device_common.cuh"
 
@@ -273,6 +274,9 @@ struct PCfg {
   // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
   // the per-K-block partials of the FP32-scale path (promotion latency slack).
   static constexpr int NACC = NACC_;
+  // FP32-scale path: the partial buffers of one unit form a slot with a single
+  // full/empty handshake between the MMA warp and the promotion warps
+  static constexpr int NSLOT = kF32S ? NACC / KPU : NACC;
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
   static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
   static constexpr int SFB_RING_BYTES = kMX ? SFB_ROWS * 4 : 0;
@@ -681,7 +685,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
               if (j < nk) {
                 const int kb = kb0 + j;
                 // FP32 scales: K block j of the unit has its own partial buffer
-                const int buf = C::kF32S ? (acc + j) % C::NACC : acc;
+                // in the unit's slot
+                const int buf = C::kF32S ? acc * C::KPU + j : acc;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                 const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
                 const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
@@ -695,15 +700,15 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
                   tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), id,
                                      sf_col, sf_col + 4, accum);
                 }
-                if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + buf), pair_mask);
               }
             }
+            if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
             tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + unit), all_mask);
             if (group_end) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + gctr % C::SF_SLOTS), pair_mask);
           }
           __syncwarp();
           if (group_end) ++gctr;
-          if constexpr (C::kF32S) acc = (acc + nk) % C::NACC;
+          if constexpr (C::kF32S) acc = (acc + 1) % C::NSLOT;
           if (++unit == C::UNITS) unit = 0;
         }
         if constexpr (!C::kF32S) {
@@ -838,11 +843,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
           const int nk = min(C::KPU, nkb - kb0);
           if constexpr (C::kF32S) {
-            // every partial buffer the unit writes has been drained by the promotion
-            for (int j = 0; j < nk; ++j) {
-              if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
-              if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
-            }
+            // the slot of partial buffers the unit writes has been drained by the promotion
+            if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
+            if (++acc == C::NSLOT) { acc = 0; acc_phase ^= 1u; }
           }
           if constexpr (C::kMX) {
             if (ok && kb0 % 4 == 0)
@@ -928,13 +931,89 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     const int nkb128 = K / 128;
     const int nnb = (N + 127) / 128;
     const int ld_a = (M + 3) / 4 * 4;
-    int pbuf = 0;
+    const int r = static_cast<int>(q * 32 + lane);
+    // The scale stream walks the same tiles and units as the promotion below, one
+    // unit earlier, with plain global loads into registers (the MMAs keep shared
+    // memory busy, so scales do not go through it).  Rows past the tile's valid
+    // rows and columns past N load nothing (zero scales).
+    int s_t = cluster_id;
+    int s_kb0 = 0;
+    const float* s_pa = nullptr;  // null: no tile left, or row past the valid rows
+    const float* s_pb = nullptr;  // null: columns past N
+    auto stream_seek = [&]() {  // first tile at or after s_t that this CTA works on
+      s_pa = nullptr;
+      s_pb = nullptr;
+      for (; s_t < num_tiles; s_t += num_clusters) {
+        Tile st;
+        if (!get_tile(s_t, st)) continue;
+        const int c0 = st.n_blk * BN + h * HALF;
+        if (r < st.row_limit)
+          s_pa = args.sfa_f32 + (SCHED == Sched::Masked ? static_cast<size_t>(st.group) * nkb128 * ld_a : 0) +
+                 (st.m_blk + r);
+        if (c0 < N) s_pb = args.sfb_f32 + (static_cast<size_t>(st.group) * nnb + c0 / 128) * nkb128;
+        return;
+      }
+    };
+    float na[C::KPU], nb[C::KPU];  // the next unit's scales, in flight
+    auto stream_fetch = [&]() {
+      if (s_t < num_tiles) {
+#pragma unroll
+        for (int j = 0; j < C::KPU; ++j) {
+          const int kb = min(s_kb0 + j, nkb - 1);  // a short tail unit repeats its last K block
+          na[j] = s_pa ? __ldg(s_pa + static_cast<size_t>(kb) * ld_a) : 0.0f;
+          nb[j] = s_pb ? __ldg(s_pb + kb) : 0.0f;
+        }
+        s_kb0 += C::KPU;
+        if (s_kb0 >= nkb) {
+          s_kb0 = 0;
+          s_t += num_clusters;
+          stream_seek();
+        }
+      }
+    };
+    stream_seek();
+    stream_fetch();
+    int pslot = 0;
     uint32_t pphase = 0;
     bool ok = true;
+    // chunks of CH columns of each partial, double-buffered across the unit: the
+    // load of chunk c + 1 is in flight while chunk c is accumulated; the slot is
+    // released as soon as its last chunk has landed
+    constexpr int CH = HALF >= 128 ? 16 : 32;
+    constexpr int NCH = HALF / CH;
+    float accv[HALF];
+    auto promote_unit = [&](auto nk_c, const float (&sc)[C::KPU], uint32_t taddr) {
+      constexpr int TOT = decltype(nk_c)::value * NCH;
+      uint32_t va[CH], vb[CH];
+      tmem_ld_chunk(taddr, va);
+      ptx::tmem_wait_ld();
+      ptx::reg_fence(va);
+#pragma unroll
+      for (int c = 0; c < TOT; ++c) {
+        uint32_t(&cur)[CH] = (c & 1) ? vb : va;
+        uint32_t(&nxt)[CH] = (c & 1) ? va : vb;
+        if (c + 1 < TOT) {
+          const int n1 = c + 1;
+          tmem_ld_chunk(taddr + static_cast<uint32_t>((n1 / NCH) * BN + CH * (n1 % NCH)), nxt);
+        } else {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + pslot));
+        }
+        const float sj = sc[c / NCH];
+        float* a0 = accv + CH * (c % NCH);
+#pragma unroll
+        for (int j = 0; j < CH; j += 2)
+          ptx::ffma2(a0[j], a0[j + 1], sj, __uint_as_float(cur[j]), __uint_as_float(cur[j + 1]));
+        if (c + 1 < TOT) {
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(nxt);
+        }
+      }
+    };
     for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
       Tile tl;
       if (!get_tile(t, tl)) continue;
-      const int r = static_cast<int>(q * 32 + lane);
       bool row_ok = r < tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {
@@ -946,56 +1025,20 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         }
       }
       const int col0 = tl.n_blk * BN + h * HALF;
-      const bool col_ok = col0 < N;
-      const float* sfa = args.sfa_f32 +
-                         (SCHED == Sched::Masked ? static_cast<size_t>(tl.group) * nkb128 * ld_a : 0) +
-                         (tl.m_blk + r);
-      const float* sfb = args.sfb_f32 +
-                         (static_cast<size_t>(tl.group) * nnb + (col_ok ? col0 / 128 : 0)) * nkb128;
-      float accv[HALF];
 #pragma unroll
       for (int i = 0; i < HALF; ++i) accv[i] = 0.0f;
-      float sa = row_ok ? __ldg(sfa) : 0.0f;
-      float sb = col_ok ? __ldg(sfb) : 0.0f;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const float s = sa * sb;
-        if (kb + 1 < nkb) {
-          sa = row_ok ? __ldg(sfa + static_cast<size_t>(kb + 1) * ld_a) : 0.0f;
-          sb = col_ok ? __ldg(sfb + kb + 1) : 0.0f;
-        }
-        if (!pwait(bar(C::BAR_ACC_FULL + pbuf), pphase, ctl)) { ok = false; break; }
+      for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
+        float sc[C::KPU];
+#pragma unroll
+        for (int j = 0; j < C::KPU; ++j) sc[j] = na[j] * nb[j];
+        stream_fetch();  // the next unit's loads run during this unit's promotion
+        if (!pwait(bar(C::BAR_ACC_FULL + pslot), pphase, ctl)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pbuf * BN + h * HALF);
-        // chunks of CH columns, double-buffered: the load of chunk c + 1 is in
-        // flight while chunk c is accumulated; the buffer is released as soon as
-        // its last chunk has landed
-        constexpr int CH = HALF >= 128 ? 16 : 32;
-        constexpr int NCH = HALF / CH;
-        uint32_t va[CH], vb[CH];
-        tmem_ld_chunk(taddr, va);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence(va);
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          uint32_t(&cur)[CH] = (c & 1) ? vb : va;
-          uint32_t(&nxt)[CH] = (c & 1) ? va : vb;
-          if (c + 1 < NCH) {
-            tmem_ld_chunk(taddr + static_cast<uint32_t>(CH * (c + 1)), nxt);
-          } else {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + pbuf));
-          }
-#pragma unroll
-          for (int j = 0; j < CH; j += 2)
-            ptx::ffma2(accv[CH * c + j], accv[CH * c + j + 1], s, __uint_as_float(cur[j]),
-                       __uint_as_float(cur[j + 1]));
-          if (c + 1 < NCH) {
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(nxt);
-          }
-        }
-        if (++pbuf == C::NACC) { pbuf = 0; pphase ^= 1u; }
+        const uint32_t taddr =
+            tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pslot * C::KPU * BN + h * HALF);
+        if (C::KPU == 1 || kb0 + C::KPU <= nkb) promote_unit(std::integral_constant<int, C::KPU>{}, sc, taddr);
+        else promote_unit(std::integral_constant<int, 1>{}, sc, taddr);
+        if (++pslot == C::NSLOT) { pslot = 0; pphase ^= 1u; }
       }
       if (!ok) break;
       if (row_ok) {
