@@ -6,8 +6,12 @@ namespace fgf8 {
 namespace {
 
 template <Sched S>
-int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
+int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles, bool thin,
                cudaStream_t stream) {
+  if constexpr (S == Sched::Dense) {
+    // at most 64 rows: 64-row A stages, more stages in flight
+    if (thin) return launch_persistent<Kind::F8F32, S, 1, 64, 12, 8, 1, 64>(a, tm, tiles, stream);
+  }
   // pairs: 128-wide tiles so that four partial buffers fit in TMEM
   if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 8, 4>(a, tm, tiles, stream);
   switch (c.bn) {
@@ -34,14 +38,16 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
+  const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn == 64;
   TensorMaps tm;
-  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta))
+  if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
+                        thin ? 64 : 128))
     return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, stream);
-    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, stream);
-    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, thin, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, false, stream);
+    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, false, stream);
   }
 }
 

@@ -72,11 +72,14 @@ constexpr int kMaxContiguousPairBlocks = 512;
 // Largest dynamic shared memory a CTA may opt into on sm_100-class parts (227 KB).
 constexpr int kMaxSmemOptin = 232448;
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, int NPAIR = 1>
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, int NPAIR = 1, int AROWS = 128>
 int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>;
   static_assert(C::SMEM_BYTES <= kMaxSmemOptin, "shared memory budget");
-  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
+  // a thin A stage is followed by at least 8 KB of the CTA's shared memory (the
+  // MMA's unused upper rows read there)
+  static_assert(C::A_ROWS == C::BM || C::STAGES * C::B_BYTES >= 64 * 128, "thin A overread");
+  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>;
   constexpr int CL = C::CLUSTER;
   static int max_clusters[64] = {};
   int dev = 0;

@@ -6,10 +6,17 @@ namespace fgf8 {
 namespace {
 
 template <Sched S>
-int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles,
+int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles, bool thin,
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
     if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 6, 2, 2>(a, tm, tiles, stream);
+    if (thin) {  // at most 64 rows: 64-row A stages, twice the stages in flight
+      switch (c.bn) {
+        case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 1, 64>(a, tm, tiles, stream);
+        case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 12, 2, 1, 64>(a, tm, tiles, stream);
+        default: return launch_persistent<Kind::MXF8, S, 1, 32, 16, 2, 1, 64>(a, tm, tiles, stream);
+      }
+    }
   }
   if (c.ncta == 2) {
     if (c.bn == 224) return launch_persistent<Kind::MXF8, S, 2, 224, 6>(a, tm, tiles, stream);
@@ -45,9 +52,10 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
+  const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn <= 64;
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
-                        128 / c.npair))
+                        thin ? 64 : 128 / c.npair))
     return 4;
   // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
   const long long kq = (a.K / 128 + 3) / 4;
@@ -60,9 +68,9 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
     return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, stream);
-    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, stream);
-    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, thin, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, false, stream);
+    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, false, stream);
   }
 }
 

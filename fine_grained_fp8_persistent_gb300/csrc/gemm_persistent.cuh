@@ -231,7 +231,7 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1>
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1, int AROWS_ = 128>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
   static constexpr int NPAIR = NPAIR_;               // pairs per cluster sharing A by multicast
@@ -251,8 +251,15 @@ struct PCfg {
   static constexpr int BK = (KIND == Kind::F16) ? 64 : 128;
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
-  static constexpr int A_BYTES = BM * 128;
-  static constexpr int A_BOX_ROWS = BM / NPAIR;      // rows of A each CTA loads
+  // Rows of A staged per K block.  A thin tile (64 rows, for a dense GEMM with at
+  // most 64 rows) halves the A stage so that twice as many stages of B are in
+  // flight; the M=128 MMA then reads its upper 64 rows from the shared memory
+  // after the stage, which only feeds accumulator rows that are never stored.
+  static constexpr int A_ROWS = AROWS_;
+  static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && NPAIR == 1 && SCHED == Sched::Dense),
+                "thin A tiles: single CTA, dense layout");
+  static constexpr int A_BYTES = A_ROWS * 128;
+  static constexpr int A_BOX_ROWS = A_ROWS / NPAIR;  // rows of A each CTA loads
   static constexpr int A_BOX_BYTES = A_BOX_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
@@ -260,7 +267,10 @@ struct PCfg {
   // warp and one stage-release commit per unit.  The FP32-scale path gives every
   // K block of a unit its own partial buffer, so it takes two K blocks per unit
   // only where four partial buffers fit (two units in flight).
-  static constexpr int KPU = kF32S ? (NACC_ >= 4 ? 2 : 1) : 2;
+  // A thin tile takes four K blocks per unit: the producer then reads 512
+  // contiguous bytes of each B row per unit (the FP32-scale one needs eight
+  // partial buffers for that).
+  static constexpr int KPU = AROWS_ < BM ? 4 : kF32S ? (NACC_ >= 4 ? 2 : 1) : 2;
   static_assert(STAGES % KPU == 0, "stages per unit");
   static constexpr int UNITS = STAGES / KPU;
   static constexpr int SF_WARPS = kMX ? 4 : 0;
@@ -277,6 +287,7 @@ struct PCfg {
   // FP32-scale path: the partial buffers of one unit form a slot with a single
   // full/empty handshake between the MMA warp and the promotion warps
   static constexpr int NSLOT = kF32S ? NACC / KPU : NACC;
+  static_assert(!kF32S || (NACC % KPU == 0 && NSLOT >= 2), "two slots of partial buffers");
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
   static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
   static constexpr int SFB_RING_BYTES = kMX ? SFB_ROWS * 4 : 0;
@@ -387,12 +398,12 @@ __device__ __forceinline__ void store_row16(void* D, size_t row_off, int col0, i
   }
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR>
-__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>::THREADS, 1)
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR, int AROWS>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -979,7 +990,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     // chunks of CH columns of each partial, double-buffered across the unit: the
     // load of chunk c + 1 is in flight while chunk c is accumulated; the slot is
     // released as soon as its last chunk has landed
-    constexpr int CH = HALF >= 128 ? 16 : 32;
+    constexpr int CH = (HALF >= 128 || C::KPU > 2) ? 16 : 32;
     constexpr int NCH = HALF / CH;
     float accv[HALF];
     auto promote_unit = [&](auto nk_c, const float (&sc)[C::KPU], uint32_t taddr) {
@@ -1036,7 +1047,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         ptx::tc_fence_after();
         const uint32_t taddr =
             tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pslot * C::KPU * BN + h * HALF);
-        if (C::KPU == 1 || kb0 + C::KPU <= nkb) promote_unit(std::integral_constant<int, C::KPU>{}, sc, taddr);
+        // a tile's last unit may hold fewer K blocks
+        const int nk = min(C::KPU, nkb - kb0);
+        if (nk == C::KPU) promote_unit(std::integral_constant<int, C::KPU>{}, sc, taddr);
+        else if (C::KPU > 3 && nk == 3) promote_unit(std::integral_constant<int, (C::KPU > 3 ? 3 : 1)>{}, sc, taddr);
+        else if (C::KPU > 2 && nk == 2) promote_unit(std::integral_constant<int, (C::KPU > 2 ? 2 : 1)>{}, sc, taddr);
         else promote_unit(std::integral_constant<int, 1>{}, sc, taddr);
         if (++pslot == C::NSLOT) { pslot = 0; pphase ^= 1u; }
       }

@@ -147,6 +147,21 @@ def test_fp8_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 0), f"f32 {tile} {M}x{N}x{K}")
 
 
+# At most 64 rows the decode tiles stage 64-row A boxes (more stages in flight):
+# ragged N, K with an odd number of 128-blocks, and more K blocks than stages.
+THIN_TILES = [(1, "1x64"), (1, "1x48"), (1, "1x32"), (0, "1x64")]
+
+
+@pytest.mark.parametrize("fmt,tile", THIN_TILES)
+@pytest.mark.parametrize("M,N,K", [(64, 448, 1920), (37, 200, 2048), (1, 96, 3968)])
+def test_fp8_thin_a_tiles(fg, dev, oracle, monkeypatch, fmt, tile, M, N, K):
+    monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+    case = _fp8_case(M, N, K, fmt, 500 + M + K)
+    out = _run_fp8(fg, dev, case, fmt, M, N)
+    assert fg.last_tile() == f"{'mxf8' if fmt else 'f8f32'} dense {tile}"
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, fmt), f"thin {tile} fmt{fmt} {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("tile", F16_TILES)
 # K = 136 and 200 leave a short last K block; 136 also gives an odd count of K blocks
 @pytest.mark.parametrize("M,N,K", [(384, 512, 640), (130, 96, 200), (520, 768, 256), (200, 256, 136)])
