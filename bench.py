@@ -496,6 +496,28 @@ def _variants(fg, dev, stream, only=None) -> dict:
         ms = timeit(lambda: fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, fmt, out=d))
         byts = m * K_IN + N_OUT * K_IN + m * N_OUT * 2 + sf_bytes(m, K_IN, fmt) + sf_bytes(N_OUT, K_IN, fmt)
         record(name, ms, 2.0 * m * N_OUT * K_IN, byts, "hbm" if m < 1024 else "tensor_fp8")
+    # the UE8M0 GEMM with its output quantized 1x128 (next layer's activations) in
+    # the epilogue, against the GEMM followed by quantize_1x128 of its bf16 output
+    if want("fused_quant") or want("gemm_then_quantize"):
+        ue = fg.SCALE_UE8M0
+        xq, sfa = fg.quantize_1x128(x, ue)
+        wq, sfb = fg.quantize_128x128(w, ue)
+        dq = torch.empty((M_TOK, N_OUT), dtype=torch.uint8, device=dev)
+        shape, dt = fg.sfa_shape(M_TOK, N_OUT, ue)
+        sfd = torch.empty(shape, dtype=dt, device=dev)
+        d = torch.empty((M_TOK, N_OUT), dtype=torch.bfloat16, device=dev)
+        byts = M_TOK * K_IN + N_OUT * K_IN + M_TOK * N_OUT + sf_bytes(M_TOK, K_IN, ue) + sf_bytes(N_OUT, K_IN, ue)
+        if want("fused_quant"):
+            ms = timeit(lambda: fg.gemm_fp8_blockscaled_quant(xq, sfa, wq, sfb, ue, ue, dq=dq, sfd=sfd))
+            record("fused_quant_ue8m0_4096x7168x7168", ms, 2.0 * M_TOK * N_OUT * K_IN, byts, "tensor_fp8")
+        if want("gemm_then_quantize"):
+            def unfused():
+                fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, ue, out=d)
+                fg.quantize_1x128(d, ue, xq=dq, sfa=sfd)
+            ms = timeit(unfused)
+            record("gemm_then_quantize_ue8m0_4096x7168x7168", ms, 2.0 * M_TOK * N_OUT * K_IN,
+                   byts + 4 * M_TOK * N_OUT, "tensor_fp8")
+        del dq, sfd, d
     del x, xq, wq
 
     # 16-bit dense 4096^3

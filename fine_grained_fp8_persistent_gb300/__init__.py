@@ -8,7 +8,7 @@ inputs) can be imported on machines where the library is not built.
 from __future__ import annotations
 
 _EXPORTS = (
-    "quantize_1x128", "quantize_128x128", "gemm_f16", "gemm_fp8_blockscaled",
+    "quantize_1x128", "quantize_128x128", "gemm_f16", "gemm_fp8_blockscaled", "gemm_fp8_blockscaled_quant",
     "grouped_fp8_contiguous", "grouped_fp8_masked", "check_status",
     "mk_alignment_for_contiguous", "sfa_bytes", "sfb_bytes", "sfa_shape", "sfb_shape",
     "set_wait_timeout_ms", "set_pdl", "selftest_wait_timeout", "last_error", "last_tile", "version", "FGF8Error", "SCALE_F32", "SCALE_UE8M0",

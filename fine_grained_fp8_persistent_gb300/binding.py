@@ -47,6 +47,7 @@ _SIGS = {
     "quantize_128x128": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gemm_f16": ([_P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "gemm_fp8_blockscaled": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gemm_fp8_blockscaled_quant": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "grouped_fp8_contiguous": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "grouped_fp8_masked": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "fgf8_mk_alignment_for_contiguous": ([], _I),
@@ -180,6 +181,24 @@ def gemm_fp8_blockscaled(aq, sfa, bq, sfb, fmt, out: torch.Tensor | None = None,
     _check(_lib.gemm_fp8_blockscaled(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(out),
                                      M, N, K, _fmt(fmt), _stream(stream)), "gemm_fp8_blockscaled")
     return out
+
+
+def gemm_fp8_blockscaled_quant(aq, sfa, bq, sfb, fmt, out_fmt, dq: torch.Tensor | None = None,
+                               sfd: torch.Tensor | None = None, stream=None):
+    """The block-scaled GEMM with its output quantized 1x128 in the epilogue:
+    returns (Dq uint8 (M, N) E4M3 codes, SFD scale table in out_fmt), equal to
+    quantize_1x128(gemm_fp8_blockscaled(...), out_fmt)."""
+    M, K = aq.shape
+    N = bq.shape[-2]
+    if dq is None:
+        dq = torch.empty((M, N), dtype=torch.uint8, device=aq.device)
+    if sfd is None:
+        shape, dt = sfa_shape(M, N, out_fmt)
+        sfd = torch.empty(shape, dtype=dt, device=aq.device)
+    _check(_lib.gemm_fp8_blockscaled_quant(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(dq),
+                                           _ptr(sfd), M, N, K, _fmt(fmt), _fmt(out_fmt), _stream(stream)),
+           "gemm_fp8_blockscaled_quant")
+    return dq, sfd
 
 
 def grouped_fp8_contiguous(aq, sfa, bq, sfb, m_indices, fmt, out: torch.Tensor | None = None,

@@ -318,6 +318,31 @@ int gemm_fp8_blockscaled(const void* Aq, const void* SFA, const void* Bq, const 
   return dispatch_fp8(a, fgf8::Sched::Dense, Aq, SFA, Bq, SFB, fmt, stream);
 }
 
+int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                               void* Dq, void* SFD, int M, int N, int K, int fmt, int out_fmt,
+                               void* stream) {
+  if (M < 0) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: M=%d", M);
+  if (int r = check_fp8_common("gemm_fp8_blockscaled_quant", N, K, fmt)) return r;
+  if (fmt != FGF8_SCALE_UE8M0)
+    return fgf8::set_error(FGF8_ERR_UNSUPPORTED,
+                           "gemm_fp8_blockscaled_quant: the input scales must be UE8M0 (block-scaled MMA)");
+  if (out_fmt != FGF8_SCALE_F32 && out_fmt != FGF8_SCALE_UE8M0)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: bad output scale format %d", out_fmt);
+  if (N % 128 != 0)
+    return fgf8::set_error(FGF8_ERR_UNSUPPORTED, "gemm_fp8_blockscaled_quant: N=%d not a multiple of 128", N);
+  if (M == 0) return FGF8_OK;
+  if (!Aq || !SFA || !Bq || !SFB || !Dq || !SFD)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: null pointer");
+  if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(Dq) || !aligned16(SFD))
+    return fgf8::set_error(FGF8_ERR_MISALIGNED, "gemm_fp8_blockscaled_quant: pointers must be 16-byte aligned");
+  fgf8::GemmArgs a;
+  if (prepare_args(a, M, N, K, 1, nullptr) != FGF8_OK) return FGF8_ERR_CUDA;
+  a.dq = static_cast<uint8_t*>(Dq);
+  a.sfd = SFD;
+  a.dq_ue8m0 = out_fmt == FGF8_SCALE_UE8M0;
+  return dispatch_fp8(a, fgf8::Sched::Dense, Aq, SFA, Bq, SFB, fmt, stream);
+}
+
 int grouped_fp8_contiguous(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
                            const int32_t* m_indices, void* D, int M, int N, int K, int G, int fmt,
                            void* stream) {

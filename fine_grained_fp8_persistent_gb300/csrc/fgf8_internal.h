@@ -37,6 +37,12 @@ struct GemmArgs {
   const uint32_t* sfb_ue8m0;  // UE8M0 path: packed weight scale words
   uint32_t* status;           // device status word
   uint64_t timeout_ns;        // bound on every barrier wait
+  // Fused output quantization (dense block-scaled GEMM on 128-wide tiles): when
+  // dq is set, D is not written; its bf16-rounded rows are quantized in 1x128
+  // groups to E4M3 codes dq [M][N] and scales sfd (the quantize_1x128 layout).
+  uint8_t* dq;
+  void* sfd;
+  int dq_ue8m0;               // 1: UE8M0 scales, 0: FP32 scales
 };
 
 struct TensorMaps {

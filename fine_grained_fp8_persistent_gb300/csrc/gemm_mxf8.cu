@@ -10,6 +10,8 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
     if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 6, 2, 2>(a, tm, tiles, stream);
+    // one 256-wide accumulator (drained by 8 epilogue warps)
+    if (c.ncta == 2 && c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1>(a, tm, tiles, stream);
     if (thin) {  // at most 64 rows: 64-row A stages, twice the stages in flight
       switch (c.bn) {
         case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 1, 64>(a, tm, tiles, stream);
@@ -35,20 +37,25 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
 
 int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void* SFA,
                      const void* Bq, const void* SFB, cudaStream_t stream) {
-  // relative tile times: see pick_cfg (the 64, 48 and 32 widths are extrapolated).
+  // relative tile times: see pick_cfg (the 64, 48 and 32 widths are extrapolated;
+  // the 256-wide pair tile, measured at 4096 x 7168 x 7168, ties the 224-wide one).
   // The contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment), else one CTA per tile.
   static const TileCfg dense_cands[] = {{2, 224, 2, 20.7}, {2, 224, 1, 18.4}, {2, 128, 1, 14.4},
                                         {1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
-                                        {1, 48, 1, 8.0},   {1, 32, 1, 6.3}};
+                                        {1, 48, 1, 8.0},   {1, 32, 1, 6.3},  {2, 256, 1, 24.2}};
   static const TileCfg pair_cands[] = {{2, 224, 1, 18.4}, {2, 128, 1, 14.4}, {1, 224, 1, 23.5},
                                        {1, 128, 1, 14.9}, {1, 64, 1, 9.1},   {1, 48, 1, 8.0},
                                        {1, 32, 1, 6.3}};
   static const TileCfg single_cands[] = {{1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
                                          {1, 48, 1, 8.0},   {1, 32, 1, 6.3}};
+  // fused output quantization: 128-wide tiles hold whole 1x128 groups
+  static const TileCfg fused_cands[] = {{2, 256, 1, 24.2}, {2, 128, 1, 14.4}, {1, 128, 1, 14.9}};
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
-  const TileCfg* cands = sched == Sched::Dense ? dense_cands : (pairs ? pair_cands : single_cands);
-  const int n = sched == Sched::Dense ? 8 : (pairs ? 7 : 5);
+  const bool fused = a.dq != nullptr;
+  if (fused && sched != Sched::Dense) return set_error(2, "fused output quantization: dense layout only");
+  const TileCfg* cands = fused ? fused_cands : sched == Sched::Dense ? dense_cands : (pairs ? pair_cands : single_cands);
+  const int n = fused ? 3 : sched == Sched::Dense ? 9 : (pairs ? 7 : 5);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;

@@ -60,6 +60,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
+#include "quant_common.cuh"
 
 namespace fgf8 {
 
@@ -274,7 +275,10 @@ struct PCfg {
   static_assert(STAGES % KPU == 0, "stages per unit");
   static constexpr int UNITS = STAGES / KPU;
   static constexpr int SF_WARPS = kMX ? 4 : 0;
-  static constexpr int EPI_WARPS = kF32S ? 8 : 4;
+  // FP32 scales: 8 promotion warps.  A single accumulator buffer (NACC = 1,
+  // 256-wide block-scaled tiles) is drained by 8 epilogue warps, two per TMEM
+  // lane quarter, so that the MMAs of the next tile wait only for the drain.
+  static constexpr int EPI_WARPS = (kF32S || NACC_ == 1) ? 8 : 4;
   static constexpr int EPI_WARP0 = 2 + SF_WARPS;
   static constexpr int RELAY_WARP = EPI_WARP0 + EPI_WARPS;
   static constexpr int THREADS = 32 * (RELAY_WARP + 1);
@@ -287,6 +291,8 @@ struct PCfg {
   // FP32-scale path: the partial buffers of one unit form a slot with a single
   // full/empty handshake between the MMA warp and the promotion warps
   static constexpr int NSLOT = kF32S ? NACC / KPU : NACC;
+  // the epilogue can quantize its own output in 1x128 groups (whole groups per tile)
+  static constexpr bool kFuseQuant = KIND == Kind::MXF8 && SCHED == Sched::Dense && BN % 128 == 0;
   static_assert(!kF32S || (NACC % KPU == 0 && NSLOT >= 2), "two slots of partial buffers");
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
   static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
@@ -303,7 +309,7 @@ struct PCfg {
   // TMEM scale slots: three where they fit next to the accumulators, so the
   // scale writers can run two groups of K blocks ahead of the MMA
   static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
-  static constexpr int SF_SLOTS = (2 * BN + 3 * SF_SLOT_COLS <= 512) ? 3 : 2;
+  static constexpr int SF_SLOTS = (NACC_ * BN + 3 * SF_SLOT_COLS <= 512) ? 3 : 2;
   static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // SF_SLOTS: slot written (even CTA)
   static constexpr int BAR_SF_FREE = BAR_SFR + SF_SLOTS;          // SF_SLOTS: slot read (each CTA)
   static constexpr int BAR_SFL = BAR_SF_FREE + SF_SLOTS;          // SF_RING: words landed (local)
@@ -332,7 +338,8 @@ struct PCfg {
                                                        : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
-  static_assert(NACC >= 2 && (kF32S || NACC == 2), "accumulator buffers");
+  static_assert(kF32S ? NACC >= 2 : (NACC == 2 || (NACC == 1 && BN == 256 && KIND == Kind::MXF8)),
+                "accumulator buffers");
   static constexpr uint32_t SF_TX = BM * 4 + BN * 4;                // bytes landing on `sf_loaded`
 };
 
@@ -396,6 +403,67 @@ __device__ __forceinline__ void store_row16(void* D, size_t row_off, int col0, i
       *reinterpret_cast<uint4*>(out + col) = w;
     }
   }
+}
+
+
+// Fused output quantization of one 128-column group of one row: `hv` holds the
+// group's values rounded to bf16 (packed in pairs, as D would be stored); writes
+// the 128 E4M3 codes and the group's scale in the quantize_1x128 layout (scale
+// table [group][ld] of floats, or packed UE8M0 words [group / 4][ld] whose byte
+// group % 4 belongs to the group).
+template <bool UE8M0>
+__device__ __forceinline__ void quantize_group_out(const uint32_t (&hv)[64], float amax, uint8_t* dq_row,
+                                                   void* sfd, size_t sf_index) {
+  const quant::GroupScale gs = quant::group_scale<UE8M0>(amax);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t h0 = hv[8 * k + 2 * i], h1 = hv[8 * k + 2 * i + 1];
+      w[i] = quant::e4m3x4<UE8M0>(__uint_as_float(h0 << 16), __uint_as_float(h0 & 0xFFFF0000u),
+                                  __uint_as_float(h1 << 16), __uint_as_float(h1 & 0xFFFF0000u), gs);
+    }
+    *reinterpret_cast<uint4*>(dq_row + 16 * k) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (UE8M0) reinterpret_cast<uint8_t*>(sfd)[sf_index] = static_cast<uint8_t>(gs.byte);
+  else reinterpret_cast<float*>(sfd)[sf_index] = gs.s;
+}
+
+// Fused output quantization of group `grp` (128 columns) of output row `grow`:
+// the codes and scale of a valid row; a zero scale for a padding row of the
+// scale table (rows M .. align4(M) - 1); and, from the row's last group, zeros in
+// the unused bytes of its UE8M0 word -- all as quantize_1x128 writes them.
+__device__ __forceinline__ void fused_group_out(const GemmArgs& args, const uint32_t (&hv)[64], float amax,
+                                                int grp, int grow, bool row_ok) {
+  const int M = args.M, N = args.N;
+  const int ld = (M + 3) / 4 * 4;
+  const int ngroups = N / 128;
+  if (grp >= ngroups) return;
+  const bool pad_row = !row_ok && grow >= M && grow < ld;
+  const bool ue = args.dq_ue8m0 != 0;
+  const size_t sf_index = ue ? (static_cast<size_t>(grp / 4) * ld + grow) * 4 + (grp % 4)
+                             : static_cast<size_t>(grp) * ld + grow;
+  if (row_ok) {
+    uint8_t* dq_row = args.dq + static_cast<size_t>(grow) * N + static_cast<size_t>(grp) * 128;
+    if (ue) quantize_group_out<true>(hv, amax, dq_row, args.sfd, sf_index);
+    else quantize_group_out<false>(hv, amax, dq_row, args.sfd, sf_index);
+  } else if (pad_row) {
+    if (ue) reinterpret_cast<uint8_t*>(args.sfd)[sf_index] = 0;
+    else reinterpret_cast<float*>(args.sfd)[sf_index] = 0.0f;
+  }
+  if (ue && grp == ngroups - 1 && (row_ok || pad_row))
+    for (int j = grp % 4 + 1; j < 4; ++j) reinterpret_cast<uint8_t*>(args.sfd)[sf_index - grp % 4 + j] = 0;
+}
+
+// 32 packed 16-bit values of one output row (16 words) -> D, columns col0..col0+31
+// clipped at N (N is a multiple of 8).
+__device__ __forceinline__ void store_row32_packed(void* D, size_t row_off, int col0, int N, const uint32_t* h) {
+  uint16_t* out = reinterpret_cast<uint16_t*>(D) + row_off;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (col0 + 8 * j < N)
+      *reinterpret_cast<uint4*>(out + col0 + 8 * j) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
 }
 
 template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR, int AROWS>
@@ -874,7 +942,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       }
       aborted = !ok;
     }
-  } else if constexpr (!C::kF32S) {
+  } else if constexpr (!C::kF32S && C::EPI_WARPS == 4) {
     // ============================================================ epilogue
     ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
     const uint32_t q = warp & 3u;
@@ -900,6 +968,42 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       }
       const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (C::kFuseQuant) {
+        if (args.dq != nullptr) {
+          // 1x128 quantization of the output rows: per 128-column group, the values
+          // rounded to bf16 exactly as D would be stored, their max |x|, the scale
+          // and the codes.  Rows between M and the scale table's padded row count
+          // get zero scales, and the last group's row fills the unused bytes of
+          // its UE8M0 word with zeros, as quantize_1x128 leaves them.
+          const int grow = tl.a_row0 + r;
+#pragma unroll 1
+          for (int g = 0; g < BN / 128; ++g) {
+            uint32_t hv[64];
+            float amax = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t v[32];
+              ptx::tmem_ld_32x32b_x32(taddr + 128u * g + 32u * c, v);
+              ptx::tmem_wait_ld();
+              ptx::reg_fence(v);
+              if (c == 3 && g == BN / 128 - 1) {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const uint32_t h = pack_2x16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), true);
+                hv[16 * c + j] = h;
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(h << 16)), fabsf(__uint_as_float(h & 0xFFFF0000u))));
+              }
+            }
+            fused_group_out(args, hv, amax, (tl.n_blk * BN) / 128 + g, grow, row_ok);
+          }
+          if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+          continue;
+        }
+      }
       // 32-column chunks, then a 16-column tail when BN is an odd multiple of 16;
       // the accumulator is released after its last load
       constexpr int NCH = BN / 32;
@@ -928,6 +1032,69 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
         if (row_ok)
           store_row16(args.D, row_off, tl.n_blk * BN + 32 * NCH, N, reinterpret_cast<const float*>(v), bf16);
+      }
+      if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+    }
+    aborted = !ok;
+  } else if constexpr (!C::kF32S) {
+    // ============================================================ drain epilogue
+    // One accumulator buffer: two warps per TMEM lane quarter each drain 128
+    // columns into registers (rounded to 16 bits) and release the buffer at once,
+    // then store them (or quantize them 1x128 when the output is quantized).
+    ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
+    constexpr int HALF = BN / 2;
+    static_assert(HALF == 128, "drain epilogue: 128 columns per warp");
+    const uint32_t q = warp & 3u;
+    const int h = static_cast<int>(warp - C::EPI_WARP0) >> 2;
+    const bool bf16 = args.out_bf16 != 0 || (C::kFuseQuant && args.dq != nullptr);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      Tile tl;
+      if (!get_tile(t, tl)) continue;
+      if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const int r = static_cast<int>(q * 32 + lane);
+      bool row_ok = r < tl.row_limit;
+      if constexpr (SCHED == Sched::Contiguous) {
+        if (row_ok) {
+          const int g = __ldg(args.m_indices + tl.a_row0 + r);
+          if (g != tl.group) {
+            if (g >= 0) atomicOr(args.status, FGF8_DEVERR_INPUT);
+            row_ok = false;
+          }
+        }
+      }
+      const uint32_t taddr =
+          tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN + h * HALF);
+      uint32_t hv[64];
+      float amax = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(v);
+        if (c == 3) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t p = pack_2x16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), bf16);
+          hv[16 * c + j] = p;
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(p << 16)), fabsf(__uint_as_float(p & 0xFFFF0000u))));
+        }
+      }
+      const int col0 = tl.n_blk * BN + h * HALF;
+      if (C::kFuseQuant && args.dq != nullptr) {
+        fused_group_out(args, hv, amax, col0 / 128, tl.a_row0 + r, row_ok);
+      } else if (row_ok) {
+        const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_row32_packed(args.D, row_off, col0 + 32 * c, N, hv + 16 * c);
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
     }

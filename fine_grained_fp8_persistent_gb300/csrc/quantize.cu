@@ -17,35 +17,14 @@
 
 #include "fgf8_internal.h"
 #include "ptx.cuh"
+#include "quant_common.cuh"
 
 namespace fgf8 {
 namespace {
 
-constexpr float kE4M3Max = 448.0f;
-
-// ceil(log2(amax / 448)) computed exactly from the bits of the FP32 quotient,
-// clamped to the UE8M0 range; 0 for amax == 0.
-__device__ __forceinline__ int ue8m0_exponent(float amax) {
-  if (amax == 0.0f) return 0;
-  const float t = __fdiv_rn(amax, kE4M3Max);
-  const uint32_t b = __float_as_uint(t);
-  const int ex = static_cast<int>((b >> 23) & 0xFFu);
-  const uint32_t man = b & 0x7FFFFFu;
-  int e;
-  if (ex != 0) {
-    e = ex - 127 + (man != 0u ? 1 : 0);
-  } else {                                   // subnormal quotient: t = man * 2^-149
-    const int msb = 31 - __clz(man);
-    e = msb - 149 + ((man & (man - 1u)) != 0u ? 1 : 0);
-  }
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-
-// 2^-e as an FP32 value, e in [-127, 127].
-__device__ __forceinline__ float exp2_neg(int e) {
-  const int be = 127 - e;
-  return be >= 1 ? __uint_as_float(static_cast<uint32_t>(be) << 23) : __uint_as_float(0x00400000u);
-}
+using quant::exp2_neg;
+using quant::kE4M3Max;
+using quant::ue8m0_exponent;
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};

@@ -123,6 +123,24 @@ FGF8_API int gemm_fp8_blockscaled(const void* Aq, const void* SFA, const void* B
                          void* D, int M, int N, int K, int fmt, void* stream);
 
 /*
+ * gemm_fp8_blockscaled_quant -- gemm_fp8_blockscaled with the next layer's
+ * activation quantization fused into its epilogue ([DG] "fine-grained
+ * quantization": activation quantization belongs in the kernel that produces
+ * the activations).  D is computed as gemm_fp8_blockscaled computes it and
+ * rounded to bf16, but instead of D the kernel writes its 1x128 quantization:
+ *   Dq  : uint8 [M][N]             E4M3 codes (output)
+ *   SFD : scale table for M rows and N columns in format out_fmt (output; the
+ *         layout quantize_1x128 writes for an M x N input, padding rows zero)
+ * The outputs are bit-identical to quantize_1x128(gemm_fp8_blockscaled(...)).
+ * Requires everything gemm_fp8_blockscaled requires, input scales fmt =
+ * FGF8_SCALE_UE8M0 (the block-scaled MMA path), N % 128 == 0.  Other inputs
+ * return FGF8_ERR_UNSUPPORTED with nothing launched.
+ */
+FGF8_API int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                               void* Dq, void* SFD, int M, int N, int K, int fmt, int out_fmt,
+                               void* stream);
+
+/*
  * grouped_fp8_contiguous -- MoE grouped GEMM, contiguous layout ([DG] "two
  * grouped layouts": the tokens of one expert are concatenated along M; N and K
  * are shared by all experts; every expert segment is padded to a multiple of

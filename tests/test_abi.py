@@ -74,6 +74,14 @@ def test_host_validation(lib):
     c = lib.grouped_fp8_contiguous
     c.argtypes = [P] * 6 + [ctypes.c_int] * 5 + [P]
     assert c(al, al, al, al, al, al, 100, 128, 128, 2, 0, None) == 2        # M % 128
+    q = lib.gemm_fp8_blockscaled_quant
+    q.argtypes = [P] * 6 + [ctypes.c_int] * 5 + [P]
+    assert q(al, al, al, al, al, al, 64, 256, 256, 0, 0, None) == 2 and "UE8M0" in _err(lib)
+    assert q(al, al, al, al, al, al, 64, 200, 256, 1, 0, None) == 2         # N % 128
+    assert q(al, al, al, al, al, al, 64, 256, 256, 1, 5, None) == 1         # output format
+    assert q(al, al, al, al, mis, al, 64, 256, 256, 1, 0, None) == 3
+    assert q(al, al, al, al, al, None, 64, 256, 256, 1, 1, None) == 1
+    assert q(None, None, None, None, None, None, 0, 256, 256, 1, 1, None) == 0
 
 
 def test_size_helpers(lib):

@@ -122,7 +122,7 @@ def test_host_validation_errors(fg, dev):
 # Every tile configuration the launchers can pick, forced through FGF8_FORCE_TILE
 # as "<CTAs per cluster>x<BN>": one CTA per tile, a CTA pair (M = 256, B split
 # across the pair), or two pairs sharing A by TMA multicast.
-MXF8_TILES = ["4x224", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
+MXF8_TILES = ["4x224", "2x256", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
 F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
 F16_TILES = ["4x256", "2x256", "2x224", "1x128"]
 
