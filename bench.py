@@ -510,6 +510,14 @@ def _variants(fg, dev, stream, only=None) -> dict:
         if want("fused_quant"):
             ms = timeit(lambda: fg.gemm_fp8_blockscaled_quant(xq, sfa, wq, sfb, ue, ue, dq=dq, sfd=sfd))
             record("fused_quant_ue8m0_4096x7168x7168", ms, 2.0 * M_TOK * N_OUT * K_IN, byts, "tensor_fp8")
+            f32 = fg.SCALE_F32
+            xq32, sfa32 = fg.quantize_1x128(x, f32)
+            wq32, sfb32 = fg.quantize_128x128(w, f32)
+            ms = timeit(lambda: fg.gemm_fp8_blockscaled_quant(xq32, sfa32, wq32, sfb32, f32, ue, dq=dq, sfd=sfd))
+            record("fused_quant_f32scale_4096x7168x7168", ms, 2.0 * M_TOK * N_OUT * K_IN,
+                   byts - sf_bytes(M_TOK, K_IN, ue) - sf_bytes(N_OUT, K_IN, ue)
+                   + sf_bytes(M_TOK, K_IN, f32) + sf_bytes(N_OUT, K_IN, f32), "tensor_fp8")
+            del xq32, wq32
         if want("gemm_then_quantize"):
             def unfused():
                 fg.gemm_fp8_blockscaled(xq, sfa, wq, sfb, ue, out=d)

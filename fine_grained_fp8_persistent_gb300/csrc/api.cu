@@ -323,9 +323,6 @@ int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, 
                                void* stream) {
   if (M < 0) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: M=%d", M);
   if (int r = check_fp8_common("gemm_fp8_blockscaled_quant", N, K, fmt)) return r;
-  if (fmt != FGF8_SCALE_UE8M0)
-    return fgf8::set_error(FGF8_ERR_UNSUPPORTED,
-                           "gemm_fp8_blockscaled_quant: the input scales must be UE8M0 (block-scaled MMA)");
   if (out_fmt != FGF8_SCALE_F32 && out_fmt != FGF8_SCALE_UE8M0)
     return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: bad output scale format %d", out_fmt);
   if (N % 128 != 0)

@@ -9,6 +9,8 @@ template <Sched S>
 int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles, bool thin,
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
+    // output quantized 1x128 in the epilogue (the fused launcher picks the 256-wide tile)
+    if (a.dq != nullptr) return launch_persistent<Kind::F8F32, S, 1, 256, 4, 2, 1, 128, true>(a, tm, tiles, stream);
     // at most 64 rows: 64-row A stages, more stages in flight
     if (thin) return launch_persistent<Kind::F8F32, S, 1, 64, 12, 8, 1, 64>(a, tm, tiles, stream);
   }
@@ -32,9 +34,14 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   static const TileCfg single_cands[] = {{1, 256, 1, 34.0}, {1, 128, 1, 16.8}, {1, 64, 1, 16.0}};
   // the contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment)
+  // fused output quantization: the 256-wide tile, whose promotion warps hold whole
+  // 1x128 groups of a row
+  static const TileCfg fused_cands[] = {{1, 256, 1, 34.0}};
+  const bool fused = a.dq != nullptr;
+  if (fused && sched != Sched::Dense) return set_error(2, "fused output quantization: dense layout only");
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
-  const TileCfg* cands = pairs ? pair_cands : single_cands;
-  const int n = pairs ? 4 : 3;
+  const TileCfg* cands = fused ? fused_cands : pairs ? pair_cands : single_cands;
+  const int n = fused ? 1 : pairs ? 4 : 3;
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;

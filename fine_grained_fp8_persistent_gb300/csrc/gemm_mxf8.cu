@@ -9,6 +9,11 @@ template <Sched S>
 int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long long tiles, bool thin,
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
+    if (a.dq != nullptr) {  // output quantized 1x128 in the epilogue
+      if (c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1, 1, 128, true>(a, tm, tiles, stream);
+      if (c.ncta == 2) return launch_persistent<Kind::MXF8, S, 2, 128, 8, 2, 1, 128, true>(a, tm, tiles, stream);
+      return launch_persistent<Kind::MXF8, S, 1, 128, 6, 2, 1, 128, true>(a, tm, tiles, stream);
+    }
     if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 6, 2, 2>(a, tm, tiles, stream);
     // one 256-wide accumulator (drained by 8 epilogue warps)
     if (c.ncta == 2 && c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1>(a, tm, tiles, stream);

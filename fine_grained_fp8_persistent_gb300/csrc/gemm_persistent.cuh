@@ -232,7 +232,8 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1, int AROWS_ = 128>
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1, int AROWS_ = 128,
+          bool QOUT_ = false>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
   static constexpr int NPAIR = NPAIR_;               // pairs per cluster sharing A by multicast
@@ -291,8 +292,14 @@ struct PCfg {
   // FP32-scale path: the partial buffers of one unit form a slot with a single
   // full/empty handshake between the MMA warp and the promotion warps
   static constexpr int NSLOT = kF32S ? NACC / KPU : NACC;
-  // the epilogue can quantize its own output in 1x128 groups (whole groups per tile)
-  static constexpr bool kFuseQuant = KIND == Kind::MXF8 && SCHED == Sched::Dense && BN % 128 == 0;
+  // the epilogue can quantize its own output in 1x128 groups: every group inside
+  // one epilogue thread (block-scaled tiles 128 or 256 wide; FP32-scale tiles 256
+  // wide, whose promotion warps each hold 128 columns of a row)
+  // (QOUT: a separate instantiation, so the plain kernels carry none of it)
+  static constexpr bool kFuseQuant = QOUT_;
+  static_assert(!QOUT_ || (SCHED == Sched::Dense &&
+                           ((KIND == Kind::MXF8 && BN % 128 == 0) || (KIND == Kind::F8F32 && BN == 256))),
+                "output quantization: whole 1x128 groups per epilogue thread");
   static_assert(!kF32S || (NACC % KPU == 0 && NSLOT >= 2), "two slots of partial buffers");
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
   static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
@@ -411,31 +418,56 @@ __device__ __forceinline__ void store_row16(void* D, size_t row_off, int col0, i
 // the 128 E4M3 codes and the group's scale in the quantize_1x128 layout (scale
 // table [group][ld] of floats, or packed UE8M0 words [group / 4][ld] whose byte
 // group % 4 belongs to the group).
-template <bool UE8M0>
-__device__ __forceinline__ void quantize_group_out(const uint32_t (&hv)[64], float amax, uint8_t* dq_row,
-                                                   void* sfd, size_t sf_index) {
-  const quant::GroupScale gs = quant::group_scale<UE8M0>(amax);
+// E4M3 codes of NV values `val(0..NV-1)` (already rounded to bf16) with the
+// group's scale, stored as NV contiguous bytes at dst.
+template <bool UE8M0, int NV, typename Val>
+__device__ __forceinline__ void quantize_codes_out(const Val& val, const quant::GroupScale& gs, uint8_t* dst) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < NV / 16; ++k) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t h0 = hv[8 * k + 2 * i], h1 = hv[8 * k + 2 * i + 1];
-      w[i] = quant::e4m3x4<UE8M0>(__uint_as_float(h0 << 16), __uint_as_float(h0 & 0xFFFF0000u),
-                                  __uint_as_float(h1 << 16), __uint_as_float(h1 & 0xFFFF0000u), gs);
+      const int e = 16 * k + 4 * i;
+      w[i] = quant::e4m3x4<UE8M0>(val(e), val(e + 1), val(e + 2), val(e + 3), gs);
     }
-    *reinterpret_cast<uint4*>(dq_row + 16 * k) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + 16 * k) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// The group's 128 values come from `val(i)`, already rounded to bf16.
+template <bool UE8M0, typename Val>
+__device__ __forceinline__ void quantize_group_out(const Val& val, float amax, uint8_t* dq_row, void* sfd,
+                                                   size_t sf_index) {
+  const quant::GroupScale gs = quant::group_scale<UE8M0>(amax);
+  quantize_codes_out<UE8M0, 128>(val, gs, dq_row);
   if (UE8M0) reinterpret_cast<uint8_t*>(sfd)[sf_index] = static_cast<uint8_t>(gs.byte);
   else reinterpret_cast<float*>(sfd)[sf_index] = gs.s;
 }
+
+// x rounded to bf16 (nearest even), as an FP32 value.
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Value i of 128 bf16 values packed in pairs (low half first).
+struct PackedBf16 {
+  const uint32_t* h;
+  __device__ __forceinline__ float operator()(int i) const {
+    const uint32_t w = h[i >> 1];
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+// Value i of 128 FP32 values, rounded to bf16.
+struct RoundedF32 {
+  const float* v;
+  __device__ __forceinline__ float operator()(int i) const { return bf16_round(v[i]); }
+};
 
 // Fused output quantization of group `grp` (128 columns) of output row `grow`:
 // the codes and scale of a valid row; a zero scale for a padding row of the
 // scale table (rows M .. align4(M) - 1); and, from the row's last group, zeros in
 // the unused bytes of its UE8M0 word -- all as quantize_1x128 writes them.
-__device__ __forceinline__ void fused_group_out(const GemmArgs& args, const uint32_t (&hv)[64], float amax,
-                                                int grp, int grow, bool row_ok) {
+template <typename Val>
+__device__ __forceinline__ void fused_group_out(const GemmArgs& args, const Val& val, float amax, int grp,
+                                                int grow, bool row_ok) {
   const int M = args.M, N = args.N;
   const int ld = (M + 3) / 4 * 4;
   const int ngroups = N / 128;
@@ -446,8 +478,8 @@ __device__ __forceinline__ void fused_group_out(const GemmArgs& args, const uint
                              : static_cast<size_t>(grp) * ld + grow;
   if (row_ok) {
     uint8_t* dq_row = args.dq + static_cast<size_t>(grow) * N + static_cast<size_t>(grp) * 128;
-    if (ue) quantize_group_out<true>(hv, amax, dq_row, args.sfd, sf_index);
-    else quantize_group_out<false>(hv, amax, dq_row, args.sfd, sf_index);
+    if (ue) quantize_group_out<true>(val, amax, dq_row, args.sfd, sf_index);
+    else quantize_group_out<false>(val, amax, dq_row, args.sfd, sf_index);
   } else if (pad_row) {
     if (ue) reinterpret_cast<uint8_t*>(args.sfd)[sf_index] = 0;
     else reinterpret_cast<float*>(args.sfd)[sf_index] = 0.0f;
@@ -466,12 +498,12 @@ __device__ __forceinline__ void store_row32_packed(void* D, size_t row_off, int 
       *reinterpret_cast<uint4*>(out + col0 + 8 * j) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR, int AROWS>
-__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>::THREADS, 1)
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR, int AROWS, bool QOUT>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -969,7 +1001,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN);
       if constexpr (C::kFuseQuant) {
-        if (args.dq != nullptr) {
+        {
           // 1x128 quantization of the output rows: per 128-column group, the values
           // rounded to bf16 exactly as D would be stored, their max |x|, the scale
           // and the codes.  Rows between M and the scale table's padded row count
@@ -998,7 +1030,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
                 amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(h << 16)), fabsf(__uint_as_float(h & 0xFFFF0000u))));
               }
             }
-            fused_group_out(args, hv, amax, (tl.n_blk * BN) / 128 + g, grow, row_ok);
+            fused_group_out(args, PackedBf16{hv}, amax, (tl.n_blk * BN) / 128 + g, grow, row_ok);
           }
           if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
           continue;
@@ -1046,7 +1078,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     static_assert(HALF == 128, "drain epilogue: 128 columns per warp");
     const uint32_t q = warp & 3u;
     const int h = static_cast<int>(warp - C::EPI_WARP0) >> 2;
-    const bool bf16 = args.out_bf16 != 0 || (C::kFuseQuant && args.dq != nullptr);
+    const bool bf16 = args.out_bf16 != 0 || C::kFuseQuant;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -1068,6 +1100,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       }
       const uint32_t taddr =
           tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * BN + h * HALF);
+      const int col0 = tl.n_blk * BN + h * HALF;
       uint32_t hv[64];
       float amax = 0.0f;
 #pragma unroll
@@ -1085,12 +1118,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         for (int j = 0; j < 16; ++j) {
           const uint32_t p = pack_2x16(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]), bf16);
           hv[16 * c + j] = p;
-          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(p << 16)), fabsf(__uint_as_float(p & 0xFFFF0000u))));
+          if constexpr (C::kFuseQuant)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(p << 16)), fabsf(__uint_as_float(p & 0xFFFF0000u))));
         }
       }
-      const int col0 = tl.n_blk * BN + h * HALF;
-      if (C::kFuseQuant && args.dq != nullptr) {
-        fused_group_out(args, hv, amax, col0 / 128, tl.a_row0 + r, row_ok);
+      // everything after the drain works from registers only
+      ptx::reg_fence(hv);
+      if constexpr (C::kFuseQuant) {
+        fused_group_out(args, PackedBf16{hv}, amax, col0 / 128, tl.a_row0 + r, row_ok);  // skips groups past N
       } else if (row_ok) {
         const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
 #pragma unroll
@@ -1223,6 +1258,17 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
         if (++pslot == C::NSLOT) { pslot = 0; pphase ^= 1u; }
       }
       if (!ok) break;
+      if constexpr (C::kFuseQuant) {
+        {
+          // 1x128 quantization of the output: this warp's 128 columns of the row
+          // are one group, quantized from the accumulators rounded to bf16
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < HALF; ++j) amax = fmaxf(amax, fabsf(bf16_round(accv[j])));
+          fused_group_out(args, RoundedF32{accv}, amax, col0 / 128, tl.a_row0 + r, row_ok);
+          continue;
+        }
+      }
       if (row_ok) {
         const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
 #pragma unroll

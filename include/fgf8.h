@@ -132,9 +132,9 @@ FGF8_API int gemm_fp8_blockscaled(const void* Aq, const void* SFA, const void* B
  *   SFD : scale table for M rows and N columns in format out_fmt (output; the
  *         layout quantize_1x128 writes for an M x N input, padding rows zero)
  * The outputs are bit-identical to quantize_1x128(gemm_fp8_blockscaled(...)).
- * Requires everything gemm_fp8_blockscaled requires, input scales fmt =
- * FGF8_SCALE_UE8M0 (the block-scaled MMA path), N % 128 == 0.  Other inputs
- * return FGF8_ERR_UNSUPPORTED with nothing launched.
+ * Requires everything gemm_fp8_blockscaled requires, and N % 128 == 0 (other
+ * N return FGF8_ERR_UNSUPPORTED with nothing launched).  Either input scale
+ * format: UE8M0 runs on the block-scaled MMA, FP32 on the promoted partials.
  */
 FGF8_API int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
                                void* Dq, void* SFD, int M, int N, int K, int fmt, int out_fmt,
