@@ -21,8 +21,13 @@
 // L2 -> SMEM stream is not the bound), so the launchers only take it when forced.
 //
 // Pipeline unit.  The producer fills, and the MMA warp consumes, KPU K blocks
-// (two, one for the FP32-scale path) per full/empty handshake, so one hand-off
-// covers 8 MMAs.
+// per full/empty handshake: two (one hand-off covers 8 MMAs); for FP32 scales two
+// where four partial buffers fit, else one; four on the decode tiles.
+//
+// Decode tiles (AROWS = 64, dense GEMMs with at most 64 rows) stage 64-row A
+// boxes, so more stages of B fit, and read each weight row in 512-byte runs.
+// QOUT kernels quantize their output 1x128 in the epilogue (E4M3 codes and
+// scales in the quantize_1x128 layout) instead of storing it.
 //
 // Roles (per CTA):
 //   warp 0   TMA producer: A/B tiles into a STAGES-deep ring of 128-byte-swizzled
@@ -45,9 +50,13 @@
 //            Block-Scaled MMA: SFA/SFB live in TMEM).  Writing them from the
 //            warps keeps the copy out of the tensor pipe: a tcgen05.cp issued
 //            between MMAs stalls the MMA stream for several hundred cycles.
-//   next     epilogue (4 warps: tcgen05.ld -> cast -> store) or, for FP32 scales,
-//            promotion (8 warps: per-128-K partial from TMEM, acc += sA*sB*partial
-//            on the CUDA cores, the DeepGEMM page's promotion loop).
+//   next     epilogue: 4 warps (tcgen05.ld -> cast -> store) with two accumulator
+//            buffers; 8 warps with a single 256-column buffer (each drains 128
+//            columns into registers, releases the buffer, then stores).  For FP32
+//            scales, promotion: 8 warps, per-128-K partial from TMEM,
+//            acc += sA*sB*partial on the CUDA cores (the DeepGEMM page's
+//            promotion loop), one full/empty handshake per unit's slot of partial
+//            buffers, the scales loaded one unit ahead into registers.
 //   last     relay warp (even CTA): waits, for the MMA warp, on the unit's `full`
 //            barrier, the accumulator's `empty` barrier and the scale slot's
 //            `sf_ready`, then meets the MMA warp at the named barrier.
@@ -286,8 +295,9 @@ struct PCfg {
   static constexpr int HANDOFF_BAR = 1;              // named barrier: relay warp + MMA warp
   static constexpr int MAX_GROUPS = 1024;
 
-  // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap), more for
-  // the per-K-block partials of the FP32-scale path (promotion latency slack).
+  // TMEM accumulator buffers: 2 for a finished tile (epilogue overlap; 1 on the
+  // 256-wide block-scaled tile, drained at once), more for the per-K-block
+  // partials of the FP32-scale path (promotion latency slack).
   static constexpr int NACC = NACC_;
   // FP32-scale path: the partial buffers of one unit form a slot with a single
   // full/empty handshake between the MMA warp and the promotion warps
@@ -413,11 +423,6 @@ __device__ __forceinline__ void store_row16(void* D, size_t row_off, int col0, i
 }
 
 
-// Fused output quantization of one 128-column group of one row: `hv` holds the
-// group's values rounded to bf16 (packed in pairs, as D would be stored); writes
-// the 128 E4M3 codes and the group's scale in the quantize_1x128 layout (scale
-// table [group][ld] of floats, or packed UE8M0 words [group / 4][ld] whose byte
-// group % 4 belongs to the group).
 // E4M3 codes of NV values `val(0..NV-1)` (already rounded to bf16) with the
 // group's scale, stored as NV contiguous bytes at dst.
 template <bool UE8M0, int NV, typename Val>
@@ -434,7 +439,10 @@ __device__ __forceinline__ void quantize_codes_out(const Val& val, const quant::
   }
 }
 
-// The group's 128 values come from `val(i)`, already rounded to bf16.
+// One 128-column group of one row: its 128 values come from `val(i)`, already
+// rounded to bf16 as D would be stored; writes the 128 E4M3 codes and the group's
+// scale in the quantize_1x128 layout (scale table [group][ld] of floats, or packed
+// UE8M0 words [group / 4][ld] whose byte group % 4 belongs to the group).
 template <bool UE8M0, typename Val>
 __device__ __forceinline__ void quantize_group_out(const Val& val, float amax, uint8_t* dq_row, void* sfd,
                                                    size_t sf_index) {
