@@ -1155,15 +1155,17 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     const int r = static_cast<int>(q * 32 + lane);
     // The scale stream walks the same tiles and units as the promotion below, one
     // unit earlier, with plain global loads into registers (the MMAs keep shared
-    // memory busy, so scales do not go through it).  Rows past the tile's valid
-    // rows and columns past N load nothing (zero scales).
+    // memory busy, so scales do not go through it).  The loads are unconditional
+    // so that nothing waits for them before the next unit: a row past the tile's
+    // valid rows, or columns past N, read the table's first entries instead, and
+    // those values only reach outputs that are never stored.
     int s_t = cluster_id;
     int s_kb0 = 0;
-    const float* s_pa = nullptr;  // null: no tile left, or row past the valid rows
-    const float* s_pb = nullptr;  // null: columns past N
+    const float* s_pa = args.sfa_f32;
+    const float* s_pb = args.sfb_f32;
     auto stream_seek = [&]() {  // first tile at or after s_t that this CTA works on
-      s_pa = nullptr;
-      s_pb = nullptr;
+      s_pa = args.sfa_f32;
+      s_pb = args.sfb_f32;
       for (; s_t < num_tiles; s_t += num_clusters) {
         Tile st;
         if (!get_tile(s_t, st)) continue;
@@ -1181,8 +1183,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
 #pragma unroll
         for (int j = 0; j < C::KPU; ++j) {
           const int kb = min(s_kb0 + j, nkb - 1);  // a short tail unit repeats its last K block
-          na[j] = s_pa ? __ldg(s_pa + static_cast<size_t>(kb) * ld_a) : 0.0f;
-          nb[j] = s_pb ? __ldg(s_pb + kb) : 0.0f;
+          na[j] = __ldg(s_pa + static_cast<size_t>(kb) * ld_a);
+          nb[j] = __ldg(s_pb + kb);
         }
         s_kb0 += C::KPU;
         if (s_kb0 >= nkb) {
