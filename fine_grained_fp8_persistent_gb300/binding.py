@@ -106,6 +106,37 @@ def _u8(t: torch.Tensor) -> torch.Tensor:
     return t.view(torch.uint8) if t.dtype != torch.uint8 else t
 
 
+# The C ABI takes raw pointers and cannot see buffer sizes, so the binding checks
+# every tensor it passes against the sizes the call will touch.
+def _need(t: torch.Tensor, numel: int, itemsize: int, name: str) -> None:
+    """An input or scale table: exactly `numel` elements of `itemsize` bytes."""
+    if t.numel() != numel or t.element_size() != itemsize:
+        raise ValueError(f"{name}: expected {numel} elements of {itemsize} bytes, "
+                         f"got {t.numel()} of {t.element_size()} ({t.dtype}, {tuple(t.shape)})")
+
+
+def _need_out(t: torch.Tensor, shape: tuple, dtypes: tuple, name: str) -> None:
+    """An output: exactly this shape and one of these dtypes."""
+    if tuple(t.shape) != tuple(shape) or t.dtype not in dtypes:
+        raise ValueError(f"{name}: expected {dtypes[0]} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _numel(shape) -> int:
+    n = 1
+    for d in shape:
+        n *= d
+    return n
+
+
+def _need_fp8(aq, sfa, bq, sfb, fmt, rows: int, G: int, N: int, K: int) -> None:
+    """E4M3 operands and their scale tables for `rows` activation rows and G
+    experts of N x K weights."""
+    _need(aq, rows * K, 1, "aq")
+    _need(bq, G * N * K, 1, "bq")
+    _need(sfa, _numel(sfa_shape(rows, K, fmt)[0]), 4, "sfa")
+    _need(sfb, _numel(sfb_shape(G, N, K, fmt)[0]), 4, "sfb")
+
+
 def align4(x: int) -> int:
     return (int(x) + 3) // 4 * 4
 
@@ -129,11 +160,15 @@ def quantize_1x128(x: torch.Tensor, fmt, xq: torch.Tensor | None = None,
                    sfa: torch.Tensor | None = None, stream=None):
     """bf16 (M, K) -> (E4M3 codes uint8 (M, K), activation scale table)."""
     M, K = x.shape
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bf16")
+    shape, dt = sfa_shape(M, K, fmt)
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if sfa is None:
-        shape, dt = sfa_shape(M, K, fmt)
         sfa = torch.empty(shape, dtype=dt, device=x.device)
+    _need(xq, M * K, 1, "xq")
+    _need(sfa, _numel(shape), 4, "sfa")
     _check(_lib.quantize_1x128(_ptr(x), _ptr(_u8(xq)), _ptr(sfa), M, K, _fmt(fmt), _stream(stream)),
            "quantize_1x128")
     return xq, sfa
@@ -143,11 +178,15 @@ def quantize_128x128(w: torch.Tensor, fmt, wq: torch.Tensor | None = None,
                      sfb: torch.Tensor | None = None, stream=None):
     """bf16 (N, K) or (G, N, K) -> (E4M3 codes, weight scale table with a G axis)."""
     G, N, K = (1, *w.shape) if w.dim() == 2 else w.shape
+    if w.dtype != torch.bfloat16:
+        raise ValueError("w must be bf16")
+    shape, dt = sfb_shape(G, N, K, fmt)
     if wq is None:
         wq = torch.empty(tuple(w.shape), dtype=torch.uint8, device=w.device)
     if sfb is None:
-        shape, dt = sfb_shape(G, N, K, fmt)
         sfb = torch.empty(shape, dtype=dt, device=w.device)
+    _need(wq, G * N * K, 1, "wq")
+    _need(sfb, _numel(shape), 4, "sfb")
     _check(_lib.quantize_128x128(_ptr(w), _ptr(_u8(wq)), _ptr(sfb), G, N, K, _fmt(fmt),
                                  _stream(stream)), "quantize_128x128")
     return wq, sfb
@@ -161,9 +200,12 @@ def gemm_f16(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype | None = N
     N = b.shape[0]
     if a.dtype != b.dtype or a.dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("A and B must both be fp16 or both bf16")
+    if tuple(b.shape) != (N, K):
+        raise ValueError(f"b: expected {(N, K)}, got {tuple(b.shape)}")
     out_dtype = out_dtype or a.dtype
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _need_out(out, (M, N), (torch.float16, torch.bfloat16), "out")
     in_code = BF16 if a.dtype == torch.bfloat16 else F16
     out_code = BF16 if out.dtype == torch.bfloat16 else F16
     _check(_lib.gemm_f16(_ptr(a), _ptr(b), _ptr(out), M, N, K, in_code, out_code, _stream(stream)),
@@ -176,8 +218,10 @@ def gemm_fp8_blockscaled(aq, sfa, bq, sfb, fmt, out: torch.Tensor | None = None,
     """D (bf16, M x N) from E4M3 A (M, K) / B (N, K) with fine-grained scales."""
     M, K = aq.shape
     N = bq.shape[-2]
+    _need_fp8(aq, sfa, bq, sfb, fmt, M, 1, N, K)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    _need_out(out, (M, N), (torch.bfloat16,), "out")
     _check(_lib.gemm_fp8_blockscaled(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(out),
                                      M, N, K, _fmt(fmt), _stream(stream)), "gemm_fp8_blockscaled")
     return out
@@ -190,11 +234,14 @@ def gemm_fp8_blockscaled_quant(aq, sfa, bq, sfb, fmt, out_fmt, dq: torch.Tensor 
     quantize_1x128(gemm_fp8_blockscaled(...), out_fmt)."""
     M, K = aq.shape
     N = bq.shape[-2]
+    _need_fp8(aq, sfa, bq, sfb, fmt, M, 1, N, K)
+    shape, dt = sfa_shape(M, N, out_fmt)
     if dq is None:
         dq = torch.empty((M, N), dtype=torch.uint8, device=aq.device)
     if sfd is None:
-        shape, dt = sfa_shape(M, N, out_fmt)
         sfd = torch.empty(shape, dtype=dt, device=aq.device)
+    _need(dq, M * N, 1, "dq")
+    _need(sfd, _numel(shape), 4, "sfd")
     _check(_lib.gemm_fp8_blockscaled_quant(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(dq),
                                            _ptr(sfd), M, N, K, _fmt(fmt), _fmt(out_fmt), _stream(stream)),
            "gemm_fp8_blockscaled_quant")
@@ -206,10 +253,12 @@ def grouped_fp8_contiguous(aq, sfa, bq, sfb, m_indices, fmt, out: torch.Tensor |
     """Contiguous-layout MoE GEMM: rows of expert g use B[g]; m_indices -1 = padding."""
     M, K = aq.shape
     G, N, _ = bq.shape
+    _need_fp8(aq, sfa, bq, sfb, fmt, M, G, N, K)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
-    if m_indices.dtype != torch.int32:
-        raise ValueError("m_indices must be int32")
+    _need_out(out, (M, N), (torch.bfloat16,), "out")
+    if m_indices.dtype != torch.int32 or m_indices.numel() != M:
+        raise ValueError("m_indices must be int32 with one entry per row")
     _check(_lib.grouped_fp8_contiguous(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
                                        _ptr(m_indices), _ptr(out), M, N, K, G, _fmt(fmt),
                                        _stream(stream)), "grouped_fp8_contiguous")
@@ -221,10 +270,15 @@ def grouped_fp8_masked(aq, sfa, bq, sfb, masked_m, fmt, expected_m: int = 0,
     """Masked-layout MoE GEMM: A (G, Mmax, K); rows >= masked_m[g] are not computed."""
     G, Mmax, K = aq.shape
     N = bq.shape[1]
+    _need(aq, G * Mmax * K, 1, "aq")
+    _need(bq, G * N * K, 1, "bq")
+    _need(sfa, G * _numel(sfa_shape(Mmax, K, fmt)[0]), 4, "sfa")
+    _need(sfb, _numel(sfb_shape(G, N, K, fmt)[0]), 4, "sfb")
     if out is None:
         out = torch.empty((G, Mmax, N), dtype=torch.bfloat16, device=aq.device)
-    if masked_m.dtype != torch.int32:
-        raise ValueError("masked_m must be int32")
+    _need_out(out, (G, Mmax, N), (torch.bfloat16,), "out")
+    if masked_m.dtype != torch.int32 or masked_m.numel() != G:
+        raise ValueError("masked_m must be int32 with one entry per expert")
     _check(_lib.grouped_fp8_masked(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
                                    _ptr(masked_m), _ptr(out), G, Mmax, N, K, int(expected_m),
                                    _fmt(fmt), _stream(stream)), "grouped_fp8_masked")

@@ -143,6 +143,8 @@ def test_fused_full_size_matches_unfused(fg, dev):
 def test_fused_rejects_unsupported(fg, dev):
     case = _case(64, 512, 256, 7)
     aq, sfa, bq, sfb = (to_dev(a, dev) for a in case)
+    shape, dt = fg.sfb_shape(1, 200, 256, UE8M0)
+    sfb200 = torch.zeros(shape, dtype=dt, device=dev)
     with pytest.raises(fg.FGF8Error) as e:                                 # N not a multiple of 128
-        fg.gemm_fp8_blockscaled_quant(aq, sfa, bq.reshape(-1, 256)[:200], sfb, UE8M0, 0)
+        fg.gemm_fp8_blockscaled_quant(aq, sfa, bq.reshape(-1, 256)[:200], sfb200, UE8M0, 0)
     assert e.value.code == 2

@@ -114,8 +114,9 @@ def test_f16_mixed_output_dtype(fg, dev, oracle):
 
 def test_host_validation_errors(fg, dev):
     a = torch.zeros((16, 100), dtype=torch.uint8, device=dev)
-    with pytest.raises(fg.FGF8Error) as e:
-        fg.gemm_fp8_blockscaled(a, a, a, a, 0)
+    no_scales = torch.zeros((0,), dtype=torch.float32, device=dev)   # K = 100 has no full 128-block
+    with pytest.raises(fg.FGF8Error) as e:                           # the library rejects K % 128
+        fg.gemm_fp8_blockscaled(a, no_scales, a, no_scales, 0)
     assert e.value.code == 2
 
 
