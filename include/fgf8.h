@@ -5,8 +5,9 @@
  * What it computes: the NT GEMM D = A * B^T (the linear layer Y = X W^T) with
  * FP32 accumulation, for 16-bit operands and for E4M3 operands carrying
  * DeepSeek-V3 fine-grained scales (1x128 per token for A, 128x128 per block for
- * B), plus the contiguous and masked grouped MoE forms and the quantizers that
- * produce the E4M3 operands.  Page references name the web page and section:
+ * B), plus the contiguous and masked grouped MoE forms, the quantizers that
+ * produce the E4M3 operands, and a GEMM whose epilogue quantizes its own output
+ * for the next layer.  Page references name the web page and section:
  *   [DG]   "DeepGEMM dissected: a 300-line FP8 GEMM kernel" (pinghaoyang.com.cn)
  *   [TC5]  "GPU GEMM part 4: tcgen05 & Blackwell" (pinghaoyang.com.cn)
  *   [TIRx] "TIRx and high-performance GEMM (part 2)" (Tencent Cloud developer)
