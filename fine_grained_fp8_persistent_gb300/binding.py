@@ -87,9 +87,39 @@ def _fmt(fmt) -> int:
     return int(fmt)
 
 
-def _stream(stream=None) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+class _Stream:
+    """The stream of one library call and its device."""
+
+    def __init__(self, handle: int, device):
+        self.handle = handle
+        self.device = device
+
+
+def same_device(device, **tensors) -> None:
+    """Raise ValueError unless every given tensor lives on `device` (the launch
+    stream's device).  The C ABI sees raw pointers only: a tensor of another GPU
+    would put that GPU's memory under the kernel's tensor maps."""
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device} but the launch stream is on {device}")
+
+
+def _stream(stream=None, **tensors) -> _Stream:
+    """The launch stream (the given one, else the current stream of the tensors'
+    device), after checking that every tensor lives on its device."""
+    if stream is None:
+        first = next((t for t in tensors.values() if t is not None), None)
+        stream = torch.cuda.current_stream(None if first is None else first.device)
+    same_device(stream.device, **tensors)
+    return _Stream(stream.cuda_stream, stream.device)
+
+
+def _call(name: str, st: _Stream, *args) -> None:
+    """Run one library entry point with the stream's device current (the library
+    takes the device from cudaGetDevice) and raise FGF8Error on failure."""
+    with torch.cuda.device(st.device):
+        rc = getattr(_lib, name)(*args, st.handle)
+    _check(rc, name)
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -169,8 +199,8 @@ def quantize_1x128(x: torch.Tensor, fmt, xq: torch.Tensor | None = None,
         sfa = torch.empty(shape, dtype=dt, device=x.device)
     _need(xq, M * K, 1, "xq")
     _need(sfa, _numel(shape), 4, "sfa")
-    _check(_lib.quantize_1x128(_ptr(x), _ptr(_u8(xq)), _ptr(sfa), M, K, _fmt(fmt), _stream(stream)),
-           "quantize_1x128")
+    st = _stream(stream, x=x, xq=xq, sfa=sfa)
+    _call("quantize_1x128", st, _ptr(x), _ptr(_u8(xq)), _ptr(sfa), M, K, _fmt(fmt))
     return xq, sfa
 
 
@@ -187,8 +217,8 @@ def quantize_128x128(w: torch.Tensor, fmt, wq: torch.Tensor | None = None,
         sfb = torch.empty(shape, dtype=dt, device=w.device)
     _need(wq, G * N * K, 1, "wq")
     _need(sfb, _numel(shape), 4, "sfb")
-    _check(_lib.quantize_128x128(_ptr(w), _ptr(_u8(wq)), _ptr(sfb), G, N, K, _fmt(fmt),
-                                 _stream(stream)), "quantize_128x128")
+    st = _stream(stream, w=w, wq=wq, sfb=sfb)
+    _call("quantize_128x128", st, _ptr(w), _ptr(_u8(wq)), _ptr(sfb), G, N, K, _fmt(fmt))
     return wq, sfb
 
 
@@ -208,8 +238,8 @@ def gemm_f16(a: torch.Tensor, b: torch.Tensor, out_dtype: torch.dtype | None = N
     _need_out(out, (M, N), (torch.float16, torch.bfloat16), "out")
     in_code = BF16 if a.dtype == torch.bfloat16 else F16
     out_code = BF16 if out.dtype == torch.bfloat16 else F16
-    _check(_lib.gemm_f16(_ptr(a), _ptr(b), _ptr(out), M, N, K, in_code, out_code, _stream(stream)),
-           "gemm_f16")
+    st = _stream(stream, a=a, b=b, out=out)
+    _call("gemm_f16", st, _ptr(a), _ptr(b), _ptr(out), M, N, K, in_code, out_code)
     return out
 
 
@@ -222,8 +252,9 @@ def gemm_fp8_blockscaled(aq, sfa, bq, sfb, fmt, out: torch.Tensor | None = None,
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
     _need_out(out, (M, N), (torch.bfloat16,), "out")
-    _check(_lib.gemm_fp8_blockscaled(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(out),
-                                     M, N, K, _fmt(fmt), _stream(stream)), "gemm_fp8_blockscaled")
+    st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, out=out)
+    _call("gemm_fp8_blockscaled", st, _ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(out),
+          M, N, K, _fmt(fmt))
     return out
 
 
@@ -242,9 +273,9 @@ def gemm_fp8_blockscaled_quant(aq, sfa, bq, sfb, fmt, out_fmt, dq: torch.Tensor 
         sfd = torch.empty(shape, dtype=dt, device=aq.device)
     _need(dq, M * N, 1, "dq")
     _need(sfd, _numel(shape), 4, "sfd")
-    _check(_lib.gemm_fp8_blockscaled_quant(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(dq),
-                                           _ptr(sfd), M, N, K, _fmt(fmt), _fmt(out_fmt), _stream(stream)),
-           "gemm_fp8_blockscaled_quant")
+    st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, dq=dq, sfd=sfd)
+    _call("gemm_fp8_blockscaled_quant", st, _ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb), _ptr(dq),
+          _ptr(sfd), M, N, K, _fmt(fmt), _fmt(out_fmt))
     return dq, sfd
 
 
@@ -259,9 +290,9 @@ def grouped_fp8_contiguous(aq, sfa, bq, sfb, m_indices, fmt, out: torch.Tensor |
     _need_out(out, (M, N), (torch.bfloat16,), "out")
     if m_indices.dtype != torch.int32 or m_indices.numel() != M:
         raise ValueError("m_indices must be int32 with one entry per row")
-    _check(_lib.grouped_fp8_contiguous(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
-                                       _ptr(m_indices), _ptr(out), M, N, K, G, _fmt(fmt),
-                                       _stream(stream)), "grouped_fp8_contiguous")
+    st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, m_indices=m_indices, out=out)
+    _call("grouped_fp8_contiguous", st, _ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
+          _ptr(m_indices), _ptr(out), M, N, K, G, _fmt(fmt))
     return out
 
 
@@ -279,9 +310,9 @@ def grouped_fp8_masked(aq, sfa, bq, sfb, masked_m, fmt, expected_m: int = 0,
     _need_out(out, (G, Mmax, N), (torch.bfloat16,), "out")
     if masked_m.dtype != torch.int32 or masked_m.numel() != G:
         raise ValueError("masked_m must be int32 with one entry per expert")
-    _check(_lib.grouped_fp8_masked(_ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
-                                   _ptr(masked_m), _ptr(out), G, Mmax, N, K, int(expected_m),
-                                   _fmt(fmt), _stream(stream)), "grouped_fp8_masked")
+    st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, masked_m=masked_m, out=out)
+    _call("grouped_fp8_masked", st, _ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
+          _ptr(masked_m), _ptr(out), G, Mmax, N, K, int(expected_m), _fmt(fmt))
     return out
 
 
@@ -289,7 +320,8 @@ def grouped_fp8_masked(aq, sfa, bq, sfb, masked_m, fmt, expected_m: int = 0,
 def check_status(stream=None) -> tuple[int, int]:
     """Synchronise the stream; return (status code, raw device status bits)."""
     bits = ctypes.c_uint(0)
-    rc = _lib.fgf8_check_status(_stream(stream), ctypes.byref(bits))
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = _lib.fgf8_check_status(s.cuda_stream, ctypes.byref(bits))
     return rc, bits.value
 
 
@@ -314,7 +346,8 @@ def selftest_wait_timeout(stream=None) -> None:
     """Run the bounded-wait self-test: a wait on a barrier nothing signals, which
     must give up after the current limit and leave FGF8_ERR_DEVICE_TIMEOUT (raw bits
     0x801) for the next check_status()."""
-    _check(_lib.fgf8_selftest_wait_timeout(_stream(stream)), "fgf8_selftest_wait_timeout")
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(_lib.fgf8_selftest_wait_timeout(s.cuda_stream), "fgf8_selftest_wait_timeout")
 
 
 def set_pdl(enable: bool) -> bool:

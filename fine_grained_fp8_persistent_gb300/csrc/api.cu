@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -68,6 +69,31 @@ const DevInfo* dev_info() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every tensor pointer must be device (or managed) memory of the current device:
+// a pointer into another GPU's memory would put a peer's memory under the tensor
+// maps, and a host pointer cannot be read by TMA.  Checked before any tensor map
+// is encoded or any kernel launched.
+int check_on_device(const char* who, std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  if (int r = current_device(&dev)) return r;
+  int i = 0;
+  for (const void* p : ptrs) {
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // the failed query also sets the runtime's last error; clear it
+      return fgf8::set_error(FGF8_ERR_INVALID_ARG, "%s: pointer %d: %s", who, i, cudaGetErrorString(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+      return fgf8::set_error(FGF8_ERR_INVALID_ARG, "%s: pointer %d is not device memory", who, i);
+    if (at.type == cudaMemoryTypeDevice && at.device != dev)
+      return fgf8::set_error(FGF8_ERR_INVALID_ARG, "%s: pointer %d is on device %d, the current device is %d",
+                             who, i, at.device, dev);
+    ++i;
+  }
+  return FGF8_OK;
+}
 long long align4(long long x) { return (x + 3) / 4 * 4; }
 
 }  // namespace
@@ -235,6 +261,7 @@ int quantize_1x128(const void* X, void* Xq, void* SFA, int M, int K, int fmt, vo
   if (!X || !Xq || !SFA) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "quantize_1x128: null pointer");
   if (!aligned16(X) || !aligned16(Xq) || !aligned16(SFA))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "quantize_1x128: pointers must be 16-byte aligned");
+  if (int r = check_on_device("quantize_1x128", {X, Xq, SFA})) return r;
   return fgf8::launch_quantize_1x128(X, Xq, SFA, M, K, fmt, static_cast<cudaStream_t>(stream));
 }
 
@@ -247,6 +274,7 @@ int quantize_128x128(const void* W, void* Wq, void* SFB, int G, int N, int K, in
   if (!W || !Wq || !SFB) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "quantize_128x128: null pointer");
   if (!aligned16(W) || !aligned16(Wq) || !aligned16(SFB))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "quantize_128x128: pointers must be 16-byte aligned");
+  if (int r = check_on_device("quantize_128x128", {W, Wq, SFB})) return r;
   return fgf8::launch_quantize_128x128(W, Wq, SFB, G, N, K, fmt, static_cast<cudaStream_t>(stream));
 }
 
@@ -276,6 +304,7 @@ int gemm_f16(const void* A, const void* B, void* D, int M, int N, int K, int in_
   if (!A || !B || !D) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_f16: null pointer");
   if (!aligned16(A) || !aligned16(B) || !aligned16(D))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "gemm_f16: pointers must be 16-byte aligned");
+  if (int r = check_on_device("gemm_f16", {A, B, D})) return r;
   fgf8::GemmArgs a;
   if (prepare_args(a, M, N, K, 1, D) != FGF8_OK) return FGF8_ERR_CUDA;
   a.in_bf16 = in_dtype == FGF8_BF16;
@@ -313,6 +342,7 @@ int gemm_fp8_blockscaled(const void* Aq, const void* SFA, const void* Bq, const 
     return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled: null pointer");
   if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(D))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "gemm_fp8_blockscaled: pointers must be 16-byte aligned");
+  if (int r = check_on_device("gemm_fp8_blockscaled", {Aq, SFA, Bq, SFB, D})) return r;
   fgf8::GemmArgs a;
   if (prepare_args(a, M, N, K, 1, D) != FGF8_OK) return FGF8_ERR_CUDA;
   return dispatch_fp8(a, fgf8::Sched::Dense, Aq, SFA, Bq, SFB, fmt, stream);
@@ -332,6 +362,7 @@ int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, 
     return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp8_blockscaled_quant: null pointer");
   if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(Dq) || !aligned16(SFD))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "gemm_fp8_blockscaled_quant: pointers must be 16-byte aligned");
+  if (int r = check_on_device("gemm_fp8_blockscaled_quant", {Aq, SFA, Bq, SFB, Dq, SFD})) return r;
   fgf8::GemmArgs a;
   if (prepare_args(a, M, N, K, 1, nullptr) != FGF8_OK) return FGF8_ERR_CUDA;
   a.dq = static_cast<uint8_t*>(Dq);
@@ -356,6 +387,7 @@ int grouped_fp8_contiguous(const void* Aq, const void* SFA, const void* Bq, cons
     return fgf8::set_error(FGF8_ERR_INVALID_ARG, "grouped_fp8_contiguous: null pointer");
   if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(D))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "grouped_fp8_contiguous: pointers must be 16-byte aligned");
+  if (int r = check_on_device("grouped_fp8_contiguous", {Aq, SFA, Bq, SFB, D, m_indices})) return r;
   fgf8::GemmArgs a;
   if (prepare_args(a, M, N, K, G, D) != FGF8_OK) return FGF8_ERR_CUDA;
   a.m_indices = m_indices;
@@ -378,6 +410,7 @@ int grouped_fp8_masked(const void* Aq, const void* SFA, const void* Bq, const vo
     return fgf8::set_error(FGF8_ERR_INVALID_ARG, "grouped_fp8_masked: null pointer");
   if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(D))
     return fgf8::set_error(FGF8_ERR_MISALIGNED, "grouped_fp8_masked: pointers must be 16-byte aligned");
+  if (int r = check_on_device("grouped_fp8_masked", {Aq, SFA, Bq, SFB, D, masked_m})) return r;
   fgf8::GemmArgs a;
   if (prepare_args(a, Mmax, N, K, G, D) != FGF8_OK) return FGF8_ERR_CUDA;
   a.masked_m = masked_m;

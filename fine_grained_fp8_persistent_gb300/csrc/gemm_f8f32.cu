@@ -10,9 +10,9 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
     // output quantized 1x128 in the epilogue (the fused launcher picks the 256-wide tile)
-    if (a.dq != nullptr) return launch_persistent<Kind::F8F32, S, 1, 256, 4, 2, 1, 128, true>(a, tm, tiles, stream);
+    if (a.dq != nullptr) return launch_persistent<Kind::F8F32, S, 1, 256, 4, 2, 128, true>(a, tm, tiles, stream);
     // at most 64 rows: 64-row A stages, more stages in flight
-    if (thin) return launch_persistent<Kind::F8F32, S, 1, 64, 12, 8, 1, 64>(a, tm, tiles, stream);
+    if (thin) return launch_persistent<Kind::F8F32, S, 1, 64, 12, 8, 64>(a, tm, tiles, stream);
   }
   // pairs: 128-wide tiles so that four partial buffers fit in TMEM
   if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 8, 4>(a, tm, tiles, stream);
@@ -30,18 +30,18 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   // relative tile times (see pick_cfg), measured on M=4096, N=K=7168: the
   // 128-wide tiles and the 256-wide one take the same time per output element,
   // and the 128-wide single-CTA tile is faster on the grouped layouts
-  static const TileCfg pair_cands[] = {{2, 128, 1, 17.0}, {1, 256, 1, 34.0}, {1, 128, 1, 16.8}, {1, 64, 1, 16.0}};
-  static const TileCfg single_cands[] = {{1, 256, 1, 34.0}, {1, 128, 1, 16.8}, {1, 64, 1, 16.0}};
+  static const TileCfg pair_cands[] = {{2, 128, 17.0}, {1, 256, 34.0}, {1, 128, 16.8}, {1, 64, 16.0}};
+  static const TileCfg single_cands[] = {{1, 256, 34.0}, {1, 128, 16.8}, {1, 64, 16.0}};
   // the contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment)
   // fused output quantization: the 256-wide tile, whose promotion warps hold whole
   // 1x128 groups of a row
-  static const TileCfg fused_cands[] = {{1, 256, 1, 34.0}};
+  static const TileCfg fused_cands[] = {{1, 256, 34.0}};
   const bool fused = a.dq != nullptr;
   if (fused && sched != Sched::Dense) return set_error(2, "fused output quantization: dense layout only");
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
   const TileCfg* cands = fused ? fused_cands : pairs ? pair_cands : single_cands;
-  const int n = fused ? 1 : pairs ? 4 : 3;
+  const int n = fused ? kCount(fused_cands) : pairs ? kCount(pair_cands) : kCount(single_cands);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;

@@ -13,9 +13,12 @@ namespace fgf8 {
 struct TileCfg {
   int ncta;       // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
   int bn;         // tile width
-  int npair;      // pairs per cluster sharing A by multicast (1 or 2)
   double t_tile;  // relative time of one cluster tile (measured, see pick_cfg)
 };
+
+// Entries of a candidate table.
+template <int N>
+constexpr int kCount(const TileCfg (&)[N]) { return N; }
 
 // Tiles of the problem for a configuration, counted per cluster (masked and
 // contiguous pairs: upper bounds).
@@ -28,8 +31,7 @@ inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
     mt = (blocks + (a.G < blocks ? a.G : blocks) + 1) / 2;
   }
   const long long nt = (a.N + c.bn - 1) / c.bn;
-  const long long np = c.npair > 1 ? c.npair : 1;
-  return (s == Sched::Masked ? a.G : 1) * mt * ((nt + np - 1) / np);
+  return (s == Sched::Masked ? a.G : 1) * mt * nt;
 }
 
 // Estimated time of a configuration: waves of cluster tiles over the SMs times the
@@ -39,7 +41,7 @@ inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
 // narrowest measured ones.  A wide tile wins on large problems; narrow tiles spread
 // skinny problems over more SMs (the DeepGEMM page's unaligned BLOCK_N argument:
 // 112 vs 128 blocks on 132 SMs).
-// FGF8_FORCE_TILE="<ctas per cluster>x<bn>" (e.g. "2x224", "4x224") selects that
+// FGF8_FORCE_TILE="<ctas per cluster>x<bn>" (e.g. "2x224", "1x128") selects that
 // configuration when it is among the candidates (used by the tests to cover
 // every instantiation).
 inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
@@ -47,14 +49,13 @@ inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
     int nc = 0, bn = 0;
     if (std::sscanf(f, "%dx%d", &nc, &bn) == 2)
       for (int i = 0; i < n; ++i)
-        if (cands[i].ncta * (cands[i].npair > 1 ? cands[i].npair : 1) == nc && cands[i].bn == bn) return i;
+        if (cands[i].ncta == nc && cands[i].bn == bn) return i;
   }
   const long long sms = device_sm_count();
   int best = 0;
   double best_cost = -1.0;
   for (int i = 0; i < n; ++i) {
-    const int cl = cands[i].ncta * (cands[i].npair > 1 ? cands[i].npair : 1);
-    const long long units = sms / cl;
+    const long long units = sms / cands[i].ncta;
     const long long waves = (tile_count(a, s, cands[i]) + units - 1) / units;
     const double cost = static_cast<double>(waves) * cands[i].t_tile;
     if (best_cost < 0 || cost < best_cost) {
@@ -72,15 +73,15 @@ constexpr int kMaxContiguousPairBlocks = 512;
 // Largest dynamic shared memory a CTA may opt into on sm_100-class parts (227 KB).
 constexpr int kMaxSmemOptin = 232448;
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, int NPAIR = 1, int AROWS = 128,
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, int AROWS = 128,
           bool QOUT = false>
 int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   static_assert(C::SMEM_BYTES <= kMaxSmemOptin, "shared memory budget");
   // a thin A stage is followed by at least 8 KB of the CTA's shared memory (the
   // MMA's unused upper rows read there)
   static_assert(C::A_ROWS == C::BM || C::STAGES * C::B_BYTES >= 64 * 128, "thin A overread");
-  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>;
+  auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   if ((a.dq != nullptr) != QOUT) return set_error(2, "output quantization and kernel disagree");
   constexpr int CL = C::CLUSTER;
   static int max_clusters[64] = {};

@@ -10,18 +10,17 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
                cudaStream_t stream) {
   if constexpr (S == Sched::Dense) {
     if (a.dq != nullptr) {  // output quantized 1x128 in the epilogue
-      if (c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1, 1, 128, true>(a, tm, tiles, stream);
-      if (c.ncta == 2) return launch_persistent<Kind::MXF8, S, 2, 128, 8, 2, 1, 128, true>(a, tm, tiles, stream);
-      return launch_persistent<Kind::MXF8, S, 1, 128, 6, 2, 1, 128, true>(a, tm, tiles, stream);
+      if (c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1, 128, true>(a, tm, tiles, stream);
+      if (c.ncta == 2) return launch_persistent<Kind::MXF8, S, 2, 128, 8, 2, 128, true>(a, tm, tiles, stream);
+      return launch_persistent<Kind::MXF8, S, 1, 128, 6, 2, 128, true>(a, tm, tiles, stream);
     }
-    if (c.npair == 2) return launch_persistent<Kind::MXF8, S, 2, 224, 6, 2, 2>(a, tm, tiles, stream);
     // one 256-wide accumulator (drained by 8 epilogue warps)
     if (c.ncta == 2 && c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1>(a, tm, tiles, stream);
     if (thin) {  // at most 64 rows: 64-row A stages, twice the stages in flight
       switch (c.bn) {
-        case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 1, 64>(a, tm, tiles, stream);
-        case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 12, 2, 1, 64>(a, tm, tiles, stream);
-        default: return launch_persistent<Kind::MXF8, S, 1, 32, 16, 2, 1, 64>(a, tm, tiles, stream);
+        case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 64>(a, tm, tiles, stream);
+        case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 12, 2, 64>(a, tm, tiles, stream);
+        default: return launch_persistent<Kind::MXF8, S, 1, 32, 16, 2, 64>(a, tm, tiles, stream);
       }
     }
   }
@@ -46,28 +45,29 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
   // the 256-wide pair tile, measured at 4096 x 7168 x 7168, ties the 224-wide one).
   // The contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment), else one CTA per tile.
-  static const TileCfg dense_cands[] = {{2, 224, 2, 20.7}, {2, 224, 1, 18.4}, {2, 128, 1, 14.4},
-                                        {1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
-                                        {1, 48, 1, 8.0},   {1, 32, 1, 6.3},  {2, 256, 1, 24.2}};
-  static const TileCfg pair_cands[] = {{2, 224, 1, 18.4}, {2, 128, 1, 14.4}, {1, 224, 1, 23.5},
-                                       {1, 128, 1, 14.9}, {1, 64, 1, 9.1},   {1, 48, 1, 8.0},
-                                       {1, 32, 1, 6.3}};
-  static const TileCfg single_cands[] = {{1, 224, 1, 23.5}, {1, 128, 1, 14.9}, {1, 64, 1, 9.1},
-                                         {1, 48, 1, 8.0},   {1, 32, 1, 6.3}};
+  static const TileCfg dense_cands[] = {{2, 224, 18.4}, {2, 128, 14.4}, {1, 224, 23.5},
+                                        {1, 128, 14.9}, {1, 64, 9.1},   {1, 48, 8.0},
+                                        {1, 32, 6.3},   {2, 256, 24.2}};
+  static const TileCfg pair_cands[] = {{2, 224, 18.4}, {2, 128, 14.4}, {1, 224, 23.5},
+                                       {1, 128, 14.9}, {1, 64, 9.1},   {1, 48, 8.0},
+                                       {1, 32, 6.3}};
+  static const TileCfg single_cands[] = {{1, 224, 23.5}, {1, 128, 14.9}, {1, 64, 9.1},
+                                         {1, 48, 8.0},   {1, 32, 6.3}};
   // fused output quantization: 128-wide tiles hold whole 1x128 groups
-  static const TileCfg fused_cands[] = {{2, 256, 1, 24.2}, {2, 128, 1, 14.4}, {1, 128, 1, 14.9}};
+  static const TileCfg fused_cands[] = {{2, 256, 24.2}, {2, 128, 14.4}, {1, 128, 14.9}};
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
   const bool fused = a.dq != nullptr;
   if (fused && sched != Sched::Dense) return set_error(2, "fused output quantization: dense layout only");
   const TileCfg* cands = fused ? fused_cands : sched == Sched::Dense ? dense_cands : (pairs ? pair_cands : single_cands);
-  const int n = fused ? 3 : sched == Sched::Dense ? 9 : (pairs ? 7 : 5);
+  const int n = fused ? kCount(fused_cands)
+                : sched == Sched::Dense ? kCount(dense_cands) : (pairs ? kCount(pair_cands) : kCount(single_cands));
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
   const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn <= 64;
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
-                        thin ? 64 : 128 / c.npair))
+                        thin ? 64 : 128))
     return 4;
   // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
   const long long kq = (a.K / 128 + 3) / 4;

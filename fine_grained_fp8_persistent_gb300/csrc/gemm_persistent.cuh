@@ -12,14 +12,6 @@
 // tile cuts both its SMEM footprint and its L2->SMEM traffic per FLOP by a third,
 // which leaves room for a deeper pipeline.
 //
-// With NPAIR = 2 a cluster holds two pairs working on adjacent N tiles of the
-// same 256 rows.  Both pairs need the same A rows, so each CTA loads half of its
-// A tile and multicasts it to its counterpart in the other pair (TMA
-// .multicast::cluster): the L2 -> SMEM traffic per pair and K block drops from
-// 2*(A + B/2) to 2*(A/2 + B/2).  Measured on GB300 this variant is slower than
-// the plain pair (the four-CTA cluster spreads worse over the GPCs and the
-// L2 -> SMEM stream is not the bound), so the launchers only take it when forced.
-//
 // Pipeline unit.  The producer fills, and the MMA warp consumes, KPU K blocks
 // per full/empty handshake: two (one hand-off covers 8 MMAs); for FP32 scales two
 // where four partial buffers fit, else one; four on the decode tiles.
@@ -113,17 +105,6 @@ __device__ __forceinline__ void tma_load_ab(uint32_t dst, const CUtensorMap* m, 
   } else {
     ptx::tma_load_2d(dst, m, bar_cluster, x, y);
   }
-}
-
-// Load into this CTA's and the other pairs' shared memory at the same offset; the
-// transaction bytes land on each destination's pair-leader barrier.
-__device__ __forceinline__ void tma_load_mc_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                                 int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
-      : "memory");
 }
 
 // tcgen05 ops with the kernel-wide cta_group.
@@ -241,13 +222,11 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int NPAIR_ = 1, int AROWS_ = 128,
+template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int AROWS_ = 128,
           bool QOUT_ = false>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
-  static constexpr int NPAIR = NPAIR_;               // pairs per cluster sharing A by multicast
-  static constexpr int CLUSTER = NCTA * NPAIR;
-  static_assert(NPAIR == 1 || (NPAIR == 2 && NCTA == 2 && SCHED == Sched::Dense), "A multicast");
+  static constexpr int CLUSTER = NCTA;               // a cluster is one CTA or one CTA pair
   static constexpr int BM = 128;                    // rows per CTA
   static constexpr int TILE_M = BM * NCTA;
   static constexpr int BN = BN_;
@@ -267,11 +246,9 @@ struct PCfg {
   // flight; the M=128 MMA then reads its upper 64 rows from the shared memory
   // after the stage, which only feeds accumulator rows that are never stored.
   static constexpr int A_ROWS = AROWS_;
-  static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && NPAIR == 1 && SCHED == Sched::Dense),
+  static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && SCHED == Sched::Dense),
                 "thin A tiles: single CTA, dense layout");
   static constexpr int A_BYTES = A_ROWS * 128;
-  static constexpr int A_BOX_ROWS = A_ROWS / NPAIR;  // rows of A each CTA loads
-  static constexpr int A_BOX_BYTES = A_BOX_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
   // K blocks per pipeline unit: one full/empty handshake, one hand-off to the MMA
@@ -506,12 +483,12 @@ __device__ __forceinline__ void store_row32_packed(void* D, size_t row_off, int 
       *reinterpret_cast<uint4*>(out + col0 + 8 * j) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
 }
 
-template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int NPAIR, int AROWS, bool QOUT>
-__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>::THREADS, 1)
+template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int AROWS, bool QOUT>
+__global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
-  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAIR, AROWS, QOUT>;
+  using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -519,17 +496,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
   const uint32_t warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
   const uint32_t crank = (C::CLUSTER > 1) ? cluster_rank() : 0u;
-  const uint32_t rank = crank % NCTA;                 // rank within the pair
-  const uint32_t pair = crank / NCTA;                 // pair within the cluster
-  const uint32_t leader_rank = pair * NCTA;
+  const uint32_t rank = crank;                        // rank within the pair
   const bool leader = rank == 0;
-  // commit masks: this pair's CTAs, and every CTA of the cluster
-  const uint16_t pair_mask = static_cast<uint16_t>(((1u << NCTA) - 1u) << leader_rank);
-  const uint16_t all_mask = static_cast<uint16_t>((1u << C::CLUSTER) - 1u);
+  // commit mask: both CTAs of the pair
+  const uint16_t pair_mask = static_cast<uint16_t>((1u << NCTA) - 1u);
 
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
   // the pair leader's copy of barrier i (cluster address)
-  auto lbar = [&](int i) -> uint32_t { return NCTA == 2 ? map_to_rank(bar(i), leader_rank) : bar(i); };
+  auto lbar = [&](int i) -> uint32_t { return NCTA == 2 ? map_to_rank(bar(i), 0u) : bar(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
@@ -541,14 +515,12 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
   const int kq = (K / 128 + 3) / 4;
   const int cluster_id = static_cast<int>(blockIdx.x) / C::CLUSTER;
   const int num_clusters = static_cast<int>(gridDim.x) / C::CLUSTER;
-  const int num_nn = (num_n + NPAIR - 1) / NPAIR;     // N tiles per cluster tile row
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int u = 0; u < C::UNITS; ++u) {
       ptx::mbar_init(bar(C::BAR_FULL + u), 1);
-      // a unit is refilled once every pair that reads it has finished with it
-      ptx::mbar_init(bar(C::BAR_EMPTY + u), NPAIR);
+      ptx::mbar_init(bar(C::BAR_EMPTY + u), 1);
     }
     for (int b = 0; b < C::NACC; ++b) {
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
@@ -669,7 +641,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
     num_runs = run_expert[C::MAX_RUNS];
     num_tiles = prefix[num_runs];
   } else {
-    num_tiles = num_m * num_nn;
+    num_tiles = num_m * num_n;
   }
 
   auto get_tile = [&](int t, Tile& tl) -> bool {
@@ -709,8 +681,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
       n = local / mt;                              // M blocks sharing a B tile are adjacent
       m = local - n * mt;
     } else {
-      dense_tile(t, num_m, num_nn, 16, m, n);
-      n = n * NPAIR + static_cast<int>(pair);
+      dense_tile(t, num_m, num_n, 16, m, n);
       rows = M;
       if constexpr (SCHED == Sched::Contiguous) {
         g = __ldg(args.m_indices + m * C::TILE_M);
@@ -754,14 +725,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
           for (int j = 0; j < nk; ++j) {
             const int stage = unit * C::KPU + j;
             const int kb = kb0 + j;
-            if constexpr (NPAIR > 1) {
-              // this CTA's share of the A tile, into the same rows of every pair
-              const uint16_t mask = static_cast<uint16_t>(((1u << rank) | (1u << (rank + NCTA))));
-              tma_load_mc_pair(sbase + C::OFF_A + stage * C::A_BYTES + pair * C::A_BOX_BYTES, &tm_a, full,
-                               kb * C::BK, tl.a_row0 + static_cast<int>(pair) * C::A_BOX_ROWS, mask);
-            } else {
-              tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
-            }
+            tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
             tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
           }
         }
@@ -822,7 +786,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, NPAI
               }
             }
             if constexpr (C::kF32S) tc_commit_mc<NCTA>(bar(C::BAR_ACC_FULL + acc), pair_mask);
-            tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + unit), all_mask);
+            tc_commit_mc<NCTA>(bar(C::BAR_EMPTY + unit), pair_mask);
             if (group_end) tc_commit_mc<NCTA>(bar(C::BAR_SF_FREE + gctr % C::SF_SLOTS), pair_mask);
           }
           __syncwarp();

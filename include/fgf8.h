@@ -14,7 +14,10 @@
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates, frees or keeps them.  Each must be 16-byte aligned.
+ *     never allocates, frees or keeps them.  Each must be 16-byte aligned and
+ *     must be device (or managed) memory of the current device
+ *     (cudaGetDevice); host memory or another GPU's memory is refused with
+ *     FGF8_ERR_INVALID_ARG before anything is launched.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and returns as soon as the work is
  *     enqueued.

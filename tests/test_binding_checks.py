@@ -1,6 +1,9 @@
 """CPU checks of the Python binding's argument checks: every tensor handed to the
-C ABI as a raw pointer must have the size the call will touch.  The library is
-replaced by a recorder, so nothing reaches a GPU."""
+C ABI as a raw pointer must have the size the call will touch, and live on the
+launch stream's device.  The library is replaced by a recorder, so nothing
+reaches a GPU."""
+from types import SimpleNamespace
+
 import pytest
 import torch
 
@@ -24,7 +27,8 @@ def fg(monkeypatch):
     rec = _Recorder()
     monkeypatch.setattr(binding, "_lib", rec)
     monkeypatch.setattr(binding, "_ptr", lambda t: None if t is None else t.data_ptr())
-    monkeypatch.setattr(binding, "_stream", lambda s=None: 0)
+    monkeypatch.setattr(binding, "_stream", lambda stream=None, **t: binding._Stream(0, None))
+    monkeypatch.setattr(binding, "_call", lambda name, st, *args: rec.calls.append(name))
     binding.recorder = rec
     return binding
 
@@ -96,3 +100,16 @@ def test_grouped_checks(fg):
     with pytest.raises(ValueError, match="m_indices"):
         fg.grouped_fp8_contiguous(a2, s2, b2, t2, torch.zeros(M - 128, dtype=torch.int32), fmt)
     assert fg.recorder.calls == ["grouped_fp8_masked", "grouped_fp8_contiguous"]
+
+
+def test_tensors_on_another_device_are_rejected():
+    """Every tensor of a call must sit on the launch stream's device (a pointer
+    into another GPU's memory would reach the kernel's tensor maps)."""
+    from fine_grained_fp8_persistent_gb300 import binding
+    d0, d1 = torch.device("cuda:0"), torch.device("cuda:1")
+    on0, on1 = SimpleNamespace(device=d0), SimpleNamespace(device=d1)
+    binding.same_device(d0, aq=on0, sfa=on0, out=None)
+    with pytest.raises(ValueError, match="sfb is on cuda:1"):
+        binding.same_device(d0, aq=on0, sfb=on1)
+    with pytest.raises(ValueError, match="launch stream is on cuda:1"):
+        binding.same_device(d1, x=on0)

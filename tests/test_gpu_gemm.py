@@ -120,12 +120,35 @@ def test_host_validation_errors(fg, dev):
     assert e.value.code == 2
 
 
+def test_host_memory_is_rejected(fg, dev):
+    """The C ABI checks that every tensor pointer is memory of the current device
+    before any tensor map is encoded: host memory (pinned or pageable) is refused
+    with FGF8_ERR_INVALID_ARG and nothing is launched."""
+    import ctypes
+    M, N, K = 128, 128, 256
+    case = _fp8_case(M, N, K, 1, 9)
+    aq, sfa, bq, sfb = (to_dev(x, dev) for x in case)
+    out = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
+    host_pinned = torch.zeros_like(aq, device="cpu").pin_memory()
+    host_pageable = torch.zeros_like(aq, device="cpu")
+    lib = fg.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    for host in (host_pinned, host_pageable):
+        rc = lib.gemm_fp8_blockscaled(host.data_ptr(), sfa.data_ptr(), bq.data_ptr(), sfb.data_ptr(),
+                                      out.data_ptr(), M, N, K, 1, stream)
+        assert rc == 1 and "not device memory" in fg.last_error(), (rc, fg.last_error())
+    torch.cuda.synchronize()
+    assert int(out.view(torch.int16).abs().sum()) == 0      # nothing was written
+    rc, _ = fg.check_status()
+    assert rc == 0
+
+
 # Every tile configuration the launchers can pick, forced through FGF8_FORCE_TILE
-# as "<CTAs per cluster>x<BN>": one CTA per tile, a CTA pair (M = 256, B split
-# across the pair), or two pairs sharing A by TMA multicast.
-MXF8_TILES = ["4x224", "2x256", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
+# as "<CTAs per cluster>x<BN>": one CTA per tile, or a CTA pair (M = 256, B split
+# across the pair).
+MXF8_TILES = ["2x256", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
 F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
-F16_TILES = ["4x256", "2x256", "2x224", "1x128"]
+F16_TILES = ["2x256", "2x224", "1x128"]
 
 
 @pytest.mark.parametrize("tile", MXF8_TILES)
