@@ -247,3 +247,104 @@ def gemm_f16_entries(A, B, rows, cols) -> np.ndarray:
     out = np.empty(r.shape, dtype=np.float64)
     _load().fgo_gemm_f16_entries(_ptr(a), _ptr(b), M, N, K, _ptr(r), _ptr(c), r.size, _ptr(out))
     return out
+
+
+# --------------------------------------------------------------------------- dequantize, then one matmul
+# The block-scaled GEMM is, by definition, the GEMM of the dequantized operands
+# ("DeepGEMM dissected", section "fine-grained quantization": x = q * s per 1x128
+# group of A and per 128x128 block of B; "GPU GEMM part 4: tcgen05 & Blackwell",
+# section 6 block-scaling formula).  The functions below take that definition
+# literally: decode every code, multiply by its group's scale (both exact in
+# fp64), then one float64 matmul from numpy as the library step.  They reach the
+# triple-loop functions above up to fp64 summation order, and are what the
+# full-size parity tests compare every output element against.
+def a_scales(SFA, M: int, K: int, fmt: int) -> np.ndarray:
+    """The (M, K/128) array of activation scales held in an SFA table."""
+    nkb = K // 128
+    sf = np.asarray(SFA)
+    if fmt == SCALE_F32:
+        return sf.astype(np.float64).reshape(nkb, -1)[:, :M].T.copy()
+    b = np.ascontiguousarray(sf).view(np.uint8).reshape((nkb + 3) // 4, -1, 4)[:, :M, :]
+    e = b.transpose(1, 0, 2).reshape(M, -1)[:, :nkb].astype(np.int64) - 127   # byte kb % 4 of word kb // 4
+    return np.ldexp(1.0, e)
+
+
+def b_scales(SFB, G: int, N: int, K: int, fmt: int) -> np.ndarray:
+    """The (G, N, K/128) array of weight scales (each row n carries the scale of
+    its 128-row block) held in an SFB table."""
+    nkb = K // 128
+    sf = np.asarray(SFB)
+    if fmt == SCALE_F32:
+        blocks = sf.astype(np.float64).reshape(G, (N + 127) // 128, nkb)
+        return np.repeat(blocks, 128, axis=1)[:, :N, :]
+    b = np.ascontiguousarray(sf).view(np.uint8).reshape(G, (nkb + 3) // 4, -1, 4)[:, :, :N, :]
+    e = b.transpose(0, 2, 1, 3).reshape(G, N, -1)[:, :, :nkb].astype(np.int64) - 127
+    return np.ldexp(1.0, e)
+
+
+def dequantize_a(Aq, SFA, fmt: int) -> np.ndarray:
+    """fp64 (M, K): decode(Aq[m, k]) * sA[m, k // 128]."""
+    a = _u8(Aq)
+    M, K = a.shape
+    return e4m3_decode(a) * np.repeat(a_scales(SFA, M, K, fmt), 128, axis=1)
+
+
+def dequantize_b(Bq, SFB, fmt: int) -> np.ndarray:
+    """fp64 (G, N, K): decode(Bq[g, n, k]) * sB[g, n // 128, k // 128]."""
+    b = _u8(Bq)
+    if b.ndim == 2:
+        b = b[None]
+    G, N, K = b.shape
+    return e4m3_decode(b) * np.repeat(b_scales(SFB, G, N, K, fmt), 128, axis=2)
+
+
+def gemm_fp8_dequant(Aq, SFA, Bq, SFB, fmt: int) -> np.ndarray:
+    """D = dequant(A) @ dequant(B)^T in float64 (the dense block-scaled GEMM)."""
+    B = dequantize_b(Bq, SFB, fmt)
+    assert B.shape[0] == 1
+    return dequantize_a(Aq, SFA, fmt) @ B[0].T
+
+
+def grouped_contiguous_dequant(Aq, SFA, Bq, SFB, m_indices, fmt: int):
+    """Contiguous layout by dequantize-then-matmul per expert: (D, valid) as
+    grouped_contiguous returns them (rows of padding or of an out-of-range
+    expert: D 0, valid 0)."""
+    A = dequantize_a(Aq, SFA, fmt)
+    B = dequantize_b(Bq, SFB, fmt)
+    G, N, _ = B.shape
+    mi = np.asarray(m_indices)
+    D = np.zeros((A.shape[0], N), dtype=np.float64)
+    valid = np.zeros((A.shape[0], N), dtype=np.uint8)
+    for g in range(G):
+        rows = np.nonzero(mi == g)[0]
+        if rows.size:
+            D[rows] = A[rows] @ B[g].T
+            valid[rows] = 1
+    return D, valid
+
+
+def grouped_masked_dequant(Aq, SFA, Bq, SFB, masked_m, fmt: int):
+    """Masked layout by dequantize-then-matmul per expert: (D, valid) as
+    grouped_masked returns them (rows >= masked_m[g]: D 0, valid 0)."""
+    a = _u8(Aq)
+    G, Mmax, K = a.shape
+    sfa = np.asarray(SFA).reshape(G, -1)
+    B = dequantize_b(Bq, SFB, fmt)
+    N = B.shape[1]
+    D = np.zeros((G, Mmax, N), dtype=np.float64)
+    valid = np.zeros((G, Mmax, N), dtype=np.uint8)
+    for g in range(G):
+        m = int(min(max(int(masked_m[g]), 0), Mmax))
+        if m:
+            D[g, :m] = dequantize_a(a[g], sfa[g], fmt)[:m] @ B[g].T
+            valid[g, :m] = 1
+    return D, valid
+
+
+def gemm_f16_matmul(A, B) -> np.ndarray:
+    """D = A B^T of 16-bit operands (given as float32 holding their values) by
+    one float64 matmul: every product of two 16-bit floats is exact in fp64
+    ("TIRx and high-performance GEMM (part 2)", problem statement of the FP16
+    NT GEMM), so this is the plain definition, summed in another order than
+    gemm_f16's loop."""
+    return _f32(A).astype(np.float64) @ _f32(B).astype(np.float64).T

@@ -56,17 +56,18 @@ def test_fp8_dense_small(fg, dev, oracle, fmt, M, N, K):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("M", [64, 4096])
-def test_fp8_dense_full_size_sampled(fg, dev, oracle, fmt, M):
-    """The 7168 x 7168 weight at M = 64 (decode) and 4096 (prefill): sampled
-    entries against the oracle, plus the whole output finite."""
+def test_fp8_dense_full_size(fg, dev, oracle, fmt, M):
+    """The 7168 x 7168 weight at M = 64 (decode) and 4096 (prefill), in the
+    launch configuration the library picks for it: every output element against
+    the oracle's dequantize-then-matmul form, plus sampled entries against its
+    per-K-block triple loop."""
     N = K = 7168
     case = _fp8_case(M, N, K, fmt, 7)
     out = _run_fp8(fg, dev, case, fmt, M, N)
-    assert bool(torch.isfinite(out.float()).all())
-    r, c = sample_entries(M, N, 1500, seed=M)
-    ref = oracle.gemm_fp8_entries(*case, fmt, r, c)
-    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
-    gemm_close(got, ref, f"fp8 full M={M} fmt{fmt}")
+    got = out.float().cpu().numpy()
+    gemm_close(got, oracle.gemm_fp8_dequant(*case, fmt), f"fp8 full M={M} fmt{fmt}")
+    r, c = sample_entries(M, N, 300, seed=M)
+    gemm_close(got[r, c], oracle.gemm_fp8_entries(*case, fmt, r, c), f"fp8 full M={M} fmt{fmt} (triple loop)")
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -90,18 +91,18 @@ def test_f16_small(fg, dev, oracle, dt, M, N, K):
     gemm_close(out.float().cpu().numpy(), ref, f"f16 {M}x{N}x{K}")
 
 
-def test_f16_full_size_sampled(fg, dev, oracle):
+def test_f16_full_size(fg, dev, oracle):
+    """16-bit 4096^3: every output element against the oracle."""
     M = N = K = 4096
     a = inputs.uniform_16bit((M, K), 11)
     b = inputs.uniform_16bit((N, K), 12)
     out = fg.gemm_f16(a.to(dev), b.to(dev))
     rc, _ = fg.check_status()
     assert rc == 0
-    assert bool(torch.isfinite(out.float()).all())
-    r, c = sample_entries(M, N, 2000, seed=3)
-    ref = oracle.gemm_f16_entries(a.float().numpy(), b.float().numpy(), r, c)
-    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
-    gemm_close(got, ref, "f16 4096^3")
+    got = out.float().cpu().numpy()
+    gemm_close(got, oracle.gemm_f16_matmul(a.float().numpy(), b.float().numpy()), "f16 4096^3")
+    r, c = sample_entries(M, N, 300, seed=3)
+    gemm_close(got[r, c], oracle.gemm_f16_entries(a.float().numpy(), b.float().numpy(), r, c), "f16 (loop)")
 
 
 def test_f16_mixed_output_dtype(fg, dev, oracle):

@@ -60,8 +60,9 @@ def test_contiguous_small(fg, dev, oracle, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_contiguous_full_size_sampled(fg, dev, oracle, fmt):
-    """8 experts sharing N=4096, K=7168; token counts multinomial(8192, uniform)."""
+def test_contiguous_full_size(fg, dev, oracle, fmt):
+    """8 experts sharing N=4096, K=7168; token counts multinomial(8192, uniform):
+    every valid output element against the oracle, padding rows untouched."""
     counts = tuple(inputs.expert_counts(8192, 8, seed=0))
     N, K = 4096, 7168
     case = _contig_case(counts, N, K, fmt, 3)
@@ -69,17 +70,18 @@ def test_contiguous_full_size_sampled(fg, dev, oracle, fmt):
     rc, _ = fg.check_status()
     assert rc == 0
     m_idx, aq, sfa, bq, sfb = case
+    ref, valid = oracle.grouped_contiguous_dequant(aq, sfa, bq, sfb, m_idx, fmt)
+    o = out.float().cpu().numpy()
+    rows = m_idx >= 0
+    assert np.array_equal(valid.any(axis=1), rows)
+    gemm_close(o[rows], ref[rows], "contiguous full")
+    assert np.isnan(o[~rows]).all(), "padding rows were written"
     rng = np.random.default_rng(1)
-    valid_rows = np.flatnonzero(m_idx >= 0)
-    r = rng.choice(valid_rows, 1200)
-    c = rng.integers(0, N, 1200)
-    ref = np.array([oracle.gemm_fp8_entries(aq, sfa, bq[g], sfb[g:g + 1], fmt, [rr], [cc])[0]
-                    for rr, cc, g in zip(r, c, m_idx[r])])
-    got = out[torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)].float().cpu().numpy()
-    gemm_close(got, ref, "contiguous full")
-    pad = torch.from_numpy(np.flatnonzero(m_idx < 0)).to(dev)
-    assert bool(torch.isnan(out[pad].float()).all())
-    assert bool(torch.isfinite(out[torch.from_numpy(valid_rows).to(dev)].float()).all())
+    r = rng.choice(np.flatnonzero(rows), 200)
+    c = rng.integers(0, N, 200)
+    loop = np.array([oracle.gemm_fp8_entries(aq, sfa, bq[g], sfb[g:g + 1], fmt, [rr], [cc])[0]
+                     for rr, cc, g in zip(r, c, m_idx[r])])
+    gemm_close(o[r, c], loop, "contiguous full (triple loop)")
 
 
 # Forced tile configurations of the contiguous layout.  CTA pairs are cut per
@@ -157,8 +159,9 @@ def test_masked_small(fg, dev, oracle, fmt, masked):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_masked_full_size_sampled(fg, dev, oracle, fmt):
-    """32 experts, Mmax=256, N=7168, K=2048, valid rows uniform in [0, 256]."""
+def test_masked_full_size(fg, dev, oracle, fmt):
+    """32 experts, Mmax=256, N=7168, K=2048, valid rows uniform in [0, 256]:
+    every valid output element against the oracle, the other rows untouched."""
     G, Mmax, N, K = 32, 256, 7168, 2048
     masked = inputs.masked_rows(G, Mmax, seed=0).numpy()
     case = _masked_case(G, Mmax, N, K, fmt, 4)
@@ -166,21 +169,19 @@ def test_masked_full_size_sampled(fg, dev, oracle, fmt):
     rc, _ = fg.check_status()
     assert rc == 0
     aq, sfa, bq, sfb = case
+    ref, valid = oracle.grouped_masked_dequant(aq, sfa, bq, sfb, masked, fmt)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    gemm_close(o[v], ref[v], "masked full")
+    assert np.isnan(o[~v]).all(), "rows beyond masked_m were written"
     rng = np.random.default_rng(2)
     gs = [g for g in range(G) if masked[g] > 0]
-    g = rng.choice(gs, 1000)
+    g = rng.choice(gs, 200)
     m = np.array([rng.integers(0, masked[x]) for x in g])
-    n = rng.integers(0, N, 1000)
-    ref = np.array([oracle.gemm_fp8_entries(aq[gg], sfa[gg], bq[gg], sfb[gg:gg + 1], fmt, [mm], [nn])[0]
-                    for gg, mm, nn in zip(g, m, n)])
-    got = out[torch.from_numpy(g).to(dev), torch.from_numpy(m).to(dev),
-              torch.from_numpy(n).to(dev)].float().cpu().numpy()
-    gemm_close(got, ref, "masked full")
-    rows = torch.arange(Mmax, device=dev)[None, :]
-    vmask = rows < torch.from_numpy(masked).to(dev)[:, None]
-    o = out.float()
-    assert bool(torch.isnan(o[~vmask]).all())
-    assert bool(torch.isfinite(o[vmask]).all())
+    n = rng.integers(0, N, 200)
+    loop = np.array([oracle.gemm_fp8_entries(aq[gg], sfa[gg], bq[gg], sfb[gg:gg + 1], fmt, [mm], [nn])[0]
+                     for gg, mm, nn in zip(g, m, n)])
+    gemm_close(o[g, m, n], loop, "masked full (triple loop)")
 
 
 def test_masked_bad_count_is_reported(fg, dev):
