@@ -569,21 +569,25 @@ def _variants_tail(fg, dev, timeit, record, sf_bytes, want, out) -> dict:
     mm = inputs.masked_rows(G, MM, 10)
     am = inputs.normal_bf16((G, MM, K), 11, outliers=True).to(dev)
     bm = inputs.normal_bf16((G, N, K), 12, outliers=True).to(dev)
-    fmt = fg.SCALE_F32
-    sh, dt = fg.sfa_shape(MM, K, fmt)
-    aq = torch.empty((G, MM, K), dtype=torch.uint8, device=dev)
-    sfa = torch.empty((G, *sh), dtype=dt, device=dev)
-    for g in range(G):
-        fg.quantize_1x128(am[g], fmt, aq[g], sfa[g])
-    bq, sfb = fg.quantize_128x128(bm, fmt)
     mm_dev = mm.to(dev)
     dm = torch.empty((G, MM, N), dtype=torch.bfloat16, device=dev)
-    ms = timeit(lambda: fg.grouped_fp8_masked(aq, sfa, bq, sfb, mm_dev, fmt, out=dm))
     sm_ = int(mm.sum())
     live = int((mm > 0).sum())
-    byts = sm_ * K + live * N * K + sm_ * N * 2 + sf_bytes(sm_, K, fmt) + live * sf_bytes(N, K, fmt)
-    record(f"grouped_masked_f32scale_32x256x7168x2048_m{sm_}", ms, 2.0 * sm_ * N * K, byts, "hbm")
-    del am, bm, aq, bq, dm
+    for fmt, tag in ((fg.SCALE_F32, "f32scale"), (fg.SCALE_UE8M0, "ue8m0")):
+        name = f"grouped_masked_{tag}_32x256x7168x2048_m{sm_}"
+        if not want(name):
+            continue
+        sh, dt = fg.sfa_shape(MM, K, fmt)
+        aq = torch.empty((G, MM, K), dtype=torch.uint8, device=dev)
+        sfa = torch.empty((G, *sh), dtype=dt, device=dev)
+        for g in range(G):
+            fg.quantize_1x128(am[g], fmt, aq[g], sfa[g])
+        bq, sfb = fg.quantize_128x128(bm, fmt)
+        ms = timeit(lambda: fg.grouped_fp8_masked(aq, sfa, bq, sfb, mm_dev, fmt, out=dm))
+        byts = sm_ * K + live * N * K + sm_ * N * 2 + sf_bytes(sm_, K, fmt) + live * sf_bytes(N, K, fmt)
+        record(name, ms, 2.0 * sm_ * N * K, byts, "hbm")
+        del aq, bq
+    del am, bm, dm
     return _quantizer_variants(fg, dev, timeit, record, sf_bytes, want, out)
 
 
