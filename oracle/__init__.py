@@ -19,6 +19,8 @@ import numpy as np
 
 SCALE_F32 = 0
 SCALE_UE8M0 = 1
+FP4_MX = 0   # MXFP4: E2M1 elements, E8M0 scale per 32 along K
+FP4_NV = 1   # NVFP4: E2M1 elements, E4M3 scale per 16 along K
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fgf8_oracle.c")
@@ -70,6 +72,16 @@ def _load():
         lib.fgo_grouped_masked.argtypes = [P, P, P, P, P, L, L, L, L, I, P, P]
         lib.fgo_gemm_f16.argtypes = [P, P, L, L, L, P]
         lib.fgo_gemm_f16_entries.argtypes = [P, P, L, L, L, P, P, L, P]
+        lib.fgo_e2m1_decode.restype = ctypes.c_double
+        lib.fgo_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.fgo_e2m1_encode.restype = ctypes.c_uint8
+        lib.fgo_e2m1_encode.argtypes = [ctypes.c_double]
+        lib.fgo_e2m1_encode_array.argtypes = [P, P, L]
+        lib.fgo_e2m1_decode_array.argtypes = [P, P, L]
+        lib.fgo_fp4_scale_value.restype = ctypes.c_double
+        lib.fgo_fp4_scale_value.argtypes = [ctypes.c_uint8, I]
+        lib.fgo_quantize_fp4.argtypes = [P, L, L, I, P, P]
+        lib.fgo_gemm_fp4.argtypes = [P, P, P, P, L, L, L, I, P]
         lib.fgo_num_threads.restype = I
         lib.fgo_set_num_threads.argtypes = [I]
         _lib = lib
@@ -348,3 +360,84 @@ def gemm_f16_matmul(A, B) -> np.ndarray:
     NT GEMM), so this is the plain definition, summed in another order than
     gemm_f16's loop."""
     return _f32(A).astype(np.float64) @ _f32(B).astype(np.float64).T
+
+
+
+# --------------------------------------------------------------------------- 4-bit formats
+# MXFP4 / NVFP4 ("GPU GEMM part 4: tcgen05 & Blackwell", sections 6.1 block-scaled
+# GEMM formula, 6.3 the two formats, 7.1 packing two elements per byte along K).
+def e2m1_decode(codes) -> np.ndarray:
+    q = _u8(codes)
+    out = np.empty(q.shape, dtype=np.float64)
+    _load().fgo_e2m1_decode_array(_ptr(q), _ptr(out), q.size)
+    return out
+
+
+def e2m1_encode(values) -> np.ndarray:
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64))
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().fgo_e2m1_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def fp4_vec(fmt: int) -> int:
+    """Elements per scale along K: 32 (MXFP4) or 16 (NVFP4)."""
+    return 32 if fmt == FP4_MX else 16
+
+
+def fp4_sf_shape(R: int, K: int, fmt: int):
+    """Scale table of R rows: int32 [ceil(K / SV / 4)][align4(R)]."""
+    return ((K // fp4_vec(fmt) + 3) // 4, align4(R)), np.int32
+
+
+def quantize_fp4(X, fmt: int):
+    """X: (R, K) float32 (bf16 values).  Returns (Xq uint8 (R, K/2) packed E2M1,
+    SF int32 scale table)."""
+    x = _f32(X)
+    R, K = x.shape
+    assert K % 64 == 0
+    q = np.empty((R, K // 2), dtype=np.uint8)
+    shape, dt = fp4_sf_shape(R, K, fmt)
+    sf = np.empty(shape, dtype=dt)
+    _load().fgo_quantize_fp4(_ptr(x), R, K, fmt, _ptr(q), _ptr(sf))
+    return q, sf
+
+
+def fp4_unpack(Xq) -> np.ndarray:
+    """(R, K/2) packed bytes -> (R, K) 4-bit codes (low nibble first)."""
+    q = _u8(Xq)
+    out = np.empty((q.shape[0], q.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = q & 0xF
+    out[:, 1::2] = q >> 4
+    return out
+
+
+def fp4_scales(SF, R: int, K: int, fmt: int) -> np.ndarray:
+    """The (R, K / SV) array of scale values held in a scale table."""
+    ng = K // fp4_vec(fmt)
+    b = np.ascontiguousarray(np.asarray(SF)).view(np.uint8).reshape((ng + 3) // 4, -1, 4)[:, :R, :]
+    b = b.transpose(1, 0, 2).reshape(R, -1)[:, :ng]
+    if fmt == FP4_MX:
+        return np.ldexp(1.0, b.astype(np.int64) - 127)
+    return e4m3_decode(b)
+
+
+def dequantize_fp4(Xq, SF, fmt: int) -> np.ndarray:
+    """fp64 (R, K): decode(code[r, k]) * scale[r, k // SV]."""
+    codes = fp4_unpack(Xq)
+    R, K = codes.shape
+    return e2m1_decode(codes) * np.repeat(fp4_scales(SF, R, K, fmt), fp4_vec(fmt), axis=1)
+
+
+def gemm_fp4(Aq, SFA, Bq, SFB, fmt: int) -> np.ndarray:
+    """The block-scaled 4-bit NT GEMM term by term in fp64 (C triple loop)."""
+    a, b = _u8(Aq), _u8(Bq)
+    M, N, K = a.shape[0], b.shape[0], a.shape[1] * 2
+    D = np.empty((M, N), dtype=np.float64)
+    _load().fgo_gemm_fp4(_ptr(a), _ptr(_sf_buffer(SFA)), _ptr(b), _ptr(_sf_buffer(SFB)), M, N, K, fmt, _ptr(D))
+    return D
+
+
+def gemm_fp4_dequant(Aq, SFA, Bq, SFB, fmt: int) -> np.ndarray:
+    """The same GEMM as dequantize-then-one-float64-matmul (the full-size form)."""
+    return dequantize_fp4(Aq, SFA, fmt) @ dequantize_fp4(Bq, SFB, fmt).T

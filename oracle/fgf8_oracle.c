@@ -486,3 +486,202 @@ void fgo_set_num_threads(int n)
     (void)n;
 #endif
 }
+
+/* ========================================================================= */
+/* 4-bit block-scaled formats: MXFP4 and NVFP4                               */
+/* [TC5] section 6.1 (the block-scaled GEMM: every SV consecutive K elements */
+/* of a row share one low-precision scale), 6.3 (MXFP4: E2M1 elements, E8M0  */
+/* scale per 32; NVFP4: E2M1 elements, E4M3 scale per 16) and 7.1 (two 4-bit */
+/* elements per byte, packed along K).                                        */
+/* ========================================================================= */
+
+#define FGO_FP4_MX 0   /* E2M1 + E8M0 scale per 32 elements along K */
+#define FGO_FP4_NV 1   /* E2M1 + E4M3 scale per 16 elements along K */
+
+/*
+ * E2M1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit, no infinity or NaN
+ * ([TC5] section 3.5 lists e2m1 among the 4-bit element types).  Exponent
+ * field 0: subnormal m * 2^-1; otherwise (1 + m/2) * 2^(e-1).  Largest 6.
+ */
+double fgo_e2m1_decode(uint8_t c)
+{
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    double v = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Code (0..7) of a non-negative value that lies on the E2M1 grid. */
+static uint8_t e2m1_code_of_grid_value(double r)
+{
+    int ex;
+    double f;
+    if (r < 1.0)
+        return (uint8_t)(r * 2.0);                  /* 0 -> 0, 0.5 -> 1 */
+    f = frexp(r, &ex);                              /* r = f * 2^ex, f in [0.5, 1) */
+    /* r = (1 + m/2) * 2^(ex-1): exponent field ex - 1 + 1, m = (2f - 1) * 2 */
+    return (uint8_t)((ex << 1) | (int)((2.0 * f - 1.0) * 2.0));
+}
+
+/*
+ * Round a real value to E2M1: nearest, ties to even, finite magnitudes above 6
+ * saturate to +-6, the sign of zero is kept (the same rounding reading as the
+ * E4M3 encoder above).  The grid spacing near |v| is a power of two (0.5 below
+ * 2, then 1, then 2), so |v| / spacing is exact and nearbyint() does the only
+ * rounding.  Returns a 4-bit code.
+ */
+uint8_t fgo_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v), spacing;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7);   /* no NaN in E2M1: the method never feeds one */
+    if (a >= 6.0)
+        return (uint8_t)(sign | 0x7);
+    spacing = (a < 2.0) ? 0.5 : (a < 4.0) ? 1.0 : 2.0;
+    return (uint8_t)(sign | e2m1_code_of_grid_value(nearbyint(a / spacing) * spacing));
+}
+
+void fgo_e2m1_encode_array(const double *x, uint8_t *q, long n)
+{
+    long i;
+    for (i = 0; i < n; ++i)
+        q[i] = fgo_e2m1_encode(x[i]);
+}
+
+void fgo_e2m1_decode_array(const uint8_t *q, double *out, long n)
+{
+    long i;
+    for (i = 0; i < n; ++i)
+        out[i] = fgo_e2m1_decode(q[i]);
+}
+
+/* Elements per scale along K. */
+static long fp4_vec(int fmt) { return fmt == FGO_FP4_MX ? 32 : 16; }
+
+/*
+ * Scale byte of one group from its max |x| (FP32, the precision the kernel
+ * decides codes in).
+ *   MXFP4: the power of two 2^e with e = ceil(log2(amax / 6)) (FP32 quotient),
+ *          clamped to [-127, 127], stored as the E8M0 byte e + 127 -- the same
+ *          reading as the FP8 path's UE8M0 scales (rounding up: nothing
+ *          saturates); amax = 0 gives byte 127 (scale 1).
+ *   NVFP4: the E4M3 code of amax / 6 (FP32 quotient; nearest even, saturating
+ *          at 448); amax = 0 gives the code of 1.0.
+ */
+static uint8_t fp4_scale_byte(float amax, int fmt)
+{
+    volatile float num = amax;
+    float t;
+    if (amax == 0.0f)
+        return (uint8_t)(fmt == FGO_FP4_MX ? 127 : fgo_e4m3_encode(1.0));
+    t = num / 6.0f;
+    if (fmt == FGO_FP4_MX) {
+        int ex, e;
+        double f = frexp((double)t, &ex);
+        e = (f == 0.5) ? ex - 1 : ex;
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+        return (uint8_t)(e + 127);
+    }
+    return fgo_e4m3_encode((double)t);
+}
+
+/* Value of a scale byte. */
+double fgo_fp4_scale_value(uint8_t b, int fmt)
+{
+    return fmt == FGO_FP4_MX ? ldexp(1.0, (int)b - 127) : fgo_e4m3_decode(b);
+}
+
+/*
+ * 1 x SV block quantization of the rows of X (activations or weights alike:
+ * the scale groups run along K for both operands, [TC5] section 6.1).
+ *   X  : R x K values (bf16 values widened to float), row-major.
+ *   Xq : R x K/2 bytes, row-major; byte j of a row holds element 2j in its low
+ *        nibble and element 2j+1 in its high nibble ([TC5] section 7.1: two
+ *        4-bit elements per byte along K).
+ *   SF : uint8 view of int32[ceil(K/SV/4)][align4(R)]; byte j of word (w, r) is
+ *        the scale of group 4w+j of row r; unused bytes and rows are 0.
+ * The element code is E2M1(x * 2^-e) (exact scaling) for MXFP4 and
+ * E2M1(x / s) with an FP32 division by the decoded E4M3 scale for NVFP4; a
+ * group whose E4M3 scale is 0 (amax / 6 below the smallest subnormal) has
+ * zero codes.  K must be a multiple of 64.
+ */
+void fgo_quantize_fp4(const float *X, long R, long K, int fmt, uint8_t *Xq, void *SF)
+{
+    long sv = fp4_vec(fmt), ng = K / sv, nw = (ng + 3) / 4, ld = fgo_align4(R), r;
+    uint8_t *sf = (uint8_t *)SF;
+    memset(SF, 0, (size_t)nw * (size_t)ld * 4u);
+    memset(Xq, 0, (size_t)R * (size_t)(K / 2));
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (r = 0; r < R; ++r) {
+        long g, k;
+        for (g = 0; g < ng; ++g) {
+            const float *x = X + r * K + g * sv;
+            float amax = 0.0f;
+            uint8_t b;
+            double s;
+            for (k = 0; k < sv; ++k) {
+                float a = fabsf(x[k]);
+                if (a > amax) amax = a;
+            }
+            b = fp4_scale_byte(amax, fmt);
+            s = fgo_fp4_scale_value(b, fmt);
+            sf[((size_t)(g / 4) * (size_t)ld + (size_t)r) * 4u + (size_t)(g % 4)] = b;
+            for (k = 0; k < sv; ++k) {
+                uint8_t c;
+                if (fmt == FGO_FP4_MX) {
+                    c = fgo_e2m1_encode(ldexp((double)x[k], 127 - (int)b));
+                } else if (s == 0.0) {
+                    c = 0;
+                } else {
+                    volatile float xv = x[k];
+                    volatile float sv32 = (float)s;
+                    float qv = xv / sv32;
+                    c = fgo_e2m1_encode((double)qv);
+                }
+                {
+                    long col = g * sv + k;
+                    uint8_t *byte = Xq + r * (K / 2) + col / 2;
+                    *byte = (uint8_t)(*byte | (col % 2 ? (uint8_t)(c << 4) : c));
+                }
+            }
+        }
+    }
+}
+
+/*
+ * The block-scaled 4-bit NT GEMM, term by term as [TC5] section 6.1 writes it:
+ *   D[i][j] = sum_k (A[i][k] * SFA[i][k/SV]) * (B[j][k] * SFB[j][k/SV])
+ * in double.  Aq (M x K/2) and Bq (N x K/2) are packed as fgo_quantize_fp4
+ * writes them, SFA / SFB in its scale layout.  D is M x N row-major.
+ */
+void fgo_gemm_fp4(const uint8_t *Aq, const void *SFA, const uint8_t *Bq, const void *SFB,
+                  long M, long N, long K, int fmt, double *D)
+{
+    long sv = fp4_vec(fmt), lda = fgo_align4(M), ldb = fgo_align4(N), i;
+    const uint8_t *sa = (const uint8_t *)SFA, *sb = (const uint8_t *)SFB;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (i = 0; i < M; ++i) {
+        long j, k;
+        for (j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (k = 0; k < K; ++k) {
+                long g = k / sv;
+                uint8_t ca = (uint8_t)((Aq[i * (K / 2) + k / 2] >> (4 * (k % 2))) & 0xF);
+                uint8_t cb = (uint8_t)((Bq[j * (K / 2) + k / 2] >> (4 * (k % 2))) & 0xF);
+                double a = fgo_e2m1_decode(ca) *
+                           fgo_fp4_scale_value(sa[((size_t)(g / 4) * (size_t)lda + (size_t)i) * 4u + (size_t)(g % 4)], fmt);
+                double b = fgo_e2m1_decode(cb) *
+                           fgo_fp4_scale_value(sb[((size_t)(g / 4) * (size_t)ldb + (size_t)j) * 4u + (size_t)(g % 4)], fmt);
+                acc += a * b;
+            }
+            D[i * N + j] = acc;
+        }
+    }
+}
