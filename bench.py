@@ -460,6 +460,8 @@ def _variants(fg, dev, stream, only=None) -> dict:
         r["GB/s"] = round(byts / (ms * 1e-3) / 1e9, 1)
         if bound == "tensor_fp8":
             r["frac"] = round(r["TFLOP/s"] / fp8_peak, 4)
+        elif bound == "tensor_fp4":
+            r["frac"] = round(r["TFLOP/s"] / (6.0 * bf16_peak), 4)
         elif bound == "tensor_bf16":
             r["frac"] = round(r["TFLOP/s"] / bf16_peak, 4)
         elif bound == "hbm":
@@ -536,6 +538,26 @@ def _variants(fg, dev, stream, only=None) -> dict:
         ms = timeit(lambda: fg.gemm_f16(a, b, out=d16))
         record("f16_4096x4096x4096", ms, 2.0 * 4096 ** 3, 3 * 4096 * 4096 * 2, "tensor_bf16")
         del a, b, d16
+
+    # 4-bit block-scaled dense GEMM (MXFP4, NVFP4) on the FP8 prefill shape, and the
+    # 4-bit quantizer on the activations; FP4 peak = 6 x the bf16 peak (nominal
+    # dense 13.5 vs 2.25 PFLOP/s)
+    if want("fp4") or want("quantize_fp4"):
+        xf = inputs.normal_bf16((M_TOK, K_IN), 13, outliers=True).to(dev)
+        wf = inputs.normal_bf16((N_OUT, K_IN), 14, outliers=True).to(dev)
+        d4 = torch.empty((M_TOK, N_OUT), dtype=torch.bfloat16, device=dev)
+        for fmt, tag, sv in ((fg.FP4_MX, "mxfp4", 32), (fg.FP4_NV, "nvfp4", 16)):
+            xq4, sfa4 = fg.quantize_fp4(xf, fmt)
+            wq4, sfb4 = fg.quantize_fp4(wf, fmt)
+            if want(f"fp4_{tag}"):
+                ms = timeit(lambda: fg.gemm_fp4_blockscaled(xq4, sfa4, wq4, sfb4, fmt, out=d4))
+                byts = (M_TOK + N_OUT) * K_IN // 2 + (M_TOK + N_OUT) * K_IN // sv + M_TOK * N_OUT * 2
+                record(f"fp4_{tag}_4096x7168x7168", ms, 2.0 * M_TOK * N_OUT * K_IN, byts, "tensor_fp4")
+            if want(f"quantize_fp4_{tag}"):
+                ms = timeit(lambda: fg.quantize_fp4(xf, fmt, xq=xq4, sf=sfa4))
+                record(f"quantize_fp4_{tag}_4096x7168", ms, 0, M_TOK * K_IN * 2 + M_TOK * K_IN // 2 + M_TOK * K_IN // sv,
+                       "hbm")
+        del xf, wf, d4, xq4, wq4
 
     # grouped contiguous: 8 experts, N = 4096, K = 7168, counts multinomial(8192)
     if not want("grouped_contiguous"):

@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libfgf8.so")
 
 SCALE_F32 = 0
 SCALE_UE8M0 = 1
+FP4_MX = 0     # MXFP4: E2M1 + E8M0 scale per 32 elements along K
+FP4_NV = 1     # NVFP4: E2M1 + E4M3 scale per 16 elements along K
 F16 = 0
 BF16 = 1
 
@@ -50,6 +52,9 @@ _SIGS = {
     "gemm_fp8_blockscaled_quant": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "grouped_fp8_contiguous": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "grouped_fp8_masked": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "quantize_fp4": ([_P, _P, _P, _I, _I, _I, _P], _I),
+    "gemm_fp4_blockscaled": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "fgf8_fp4_sf_bytes": ([_I, _I, _I], _LL),
     "fgf8_mk_alignment_for_contiguous": ([], _I),
     "fgf8_sfa_bytes": ([_I, _I, _I], _LL),
     "fgf8_sfb_bytes": ([_I, _I, _I, _I], _LL),
@@ -313,6 +318,54 @@ def grouped_fp8_masked(aq, sfa, bq, sfb, masked_m, fmt, expected_m: int = 0,
     st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, masked_m=masked_m, out=out)
     _call("grouped_fp8_masked", st, _ptr(_u8(aq)), _ptr(sfa), _ptr(_u8(bq)), _ptr(sfb),
           _ptr(masked_m), _ptr(out), G, Mmax, N, K, int(expected_m), _fmt(fmt))
+    return out
+
+
+# --------------------------------------------------------------------------- 4-bit
+def _fp4(fmt) -> int:
+    if isinstance(fmt, str):
+        return {"mx": FP4_MX, "mxfp4": FP4_MX, "nv": FP4_NV, "nvfp4": FP4_NV}[fmt.lower()]
+    return int(fmt)
+
+
+def fp4_sf_shape(rows: int, K: int, fmt) -> tuple[tuple[int, ...], torch.dtype]:
+    """Scale table of quantize_fp4: int32 [ceil(K / SV / 4)][align4(rows)]."""
+    sv = 32 if _fp4(fmt) == FP4_MX else 16
+    return ((K // sv + 3) // 4, align4(rows)), torch.int32
+
+
+def quantize_fp4(x: torch.Tensor, fmt, xq: torch.Tensor | None = None, sf: torch.Tensor | None = None,
+                 stream=None):
+    """bf16 (R, K) -> (packed E2M1 codes uint8 (R, K/2), scale table), MXFP4 or NVFP4."""
+    R, K = x.shape
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bf16")
+    shape, dt = fp4_sf_shape(R, K, fmt)
+    if xq is None:
+        xq = torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(shape, dtype=dt, device=x.device)
+    _need(xq, R * (K // 2), 1, "xq")
+    _need(sf, _numel(shape), 4, "sf")
+    st = _stream(stream, x=x, xq=xq, sf=sf)
+    _call("quantize_fp4", st, _ptr(x), _ptr(xq), _ptr(sf), R, K, _fp4(fmt))
+    return xq, sf
+
+
+def gemm_fp4_blockscaled(aq, sfa, bq, sfb, fmt, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D (bf16, M x N) from packed E2M1 A (M, K/2) / B (N, K/2) with MXFP4 or NVFP4 scales."""
+    M, Kh = aq.shape
+    N = bq.shape[0]
+    K = 2 * Kh
+    _need(aq, M * Kh, 1, "aq")
+    _need(bq, N * Kh, 1, "bq")
+    _need(sfa, _numel(fp4_sf_shape(M, K, fmt)[0]), 4, "sfa")
+    _need(sfb, _numel(fp4_sf_shape(N, K, fmt)[0]), 4, "sfb")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    _need_out(out, (M, N), (torch.bfloat16,), "out")
+    st = _stream(stream, aq=aq, sfa=sfa, bq=bq, sfb=sfb, out=out)
+    _call("gemm_fp4_blockscaled", st, _ptr(aq), _ptr(sfa), _ptr(bq), _ptr(sfb), _ptr(out), M, N, K, _fp4(fmt))
     return out
 
 

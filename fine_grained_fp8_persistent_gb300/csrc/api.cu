@@ -278,6 +278,25 @@ int quantize_128x128(const void* W, void* Wq, void* SFB, int G, int N, int K, in
   return fgf8::launch_quantize_128x128(W, Wq, SFB, G, N, K, fmt, static_cast<cudaStream_t>(stream));
 }
 
+long long fgf8_fp4_sf_bytes(int R, int K, int fmt) {
+  if (R < 0 || K <= 0 || K % 64 != 0 || (fmt != FGF8_FP4_MX && fmt != FGF8_FP4_NV)) return -1;
+  const long long groups = K / (fmt == FGF8_FP4_MX ? 32 : 16);
+  return (groups + 3) / 4 * align4(R) * 4;
+}
+
+int quantize_fp4(const void* X, void* Xq, void* SF, int R, int K, int fmt, void* stream) {
+  if (R < 0 || K <= 0) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "quantize_fp4: R=%d K=%d", R, K);
+  if (K % 64 != 0) return fgf8::set_error(FGF8_ERR_UNSUPPORTED, "quantize_fp4: K=%d not a multiple of 64", K);
+  if (fmt != FGF8_FP4_MX && fmt != FGF8_FP4_NV)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "quantize_fp4: bad format %d", fmt);
+  if (R == 0) return FGF8_OK;
+  if (!X || !Xq || !SF) return fgf8::set_error(FGF8_ERR_INVALID_ARG, "quantize_fp4: null pointer");
+  if (!aligned16(X) || !aligned16(Xq) || !aligned16(SF))
+    return fgf8::set_error(FGF8_ERR_MISALIGNED, "quantize_fp4: pointers must be 16-byte aligned");
+  if (int r = check_on_device("quantize_fp4", {X, Xq, SF})) return r;
+  return fgf8::launch_quantize_fp4(X, Xq, SF, R, K, fmt, static_cast<cudaStream_t>(stream));
+}
+
 static int prepare_args(fgf8::GemmArgs& a, int M, int N, int K, int G, void* D) {
   std::memset(&a, 0, sizeof(a));
   a.M = M;
@@ -369,6 +388,25 @@ int gemm_fp8_blockscaled_quant(const void* Aq, const void* SFA, const void* Bq, 
   a.sfd = SFD;
   a.dq_ue8m0 = out_fmt == FGF8_SCALE_UE8M0;
   return dispatch_fp8(a, fgf8::Sched::Dense, Aq, SFA, Bq, SFB, fmt, stream);
+}
+
+int gemm_fp4_blockscaled(const void* Aq, const void* SFA, const void* Bq, const void* SFB, void* D, int M,
+                         int N, int K, int fmt, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp4_blockscaled: M=%d N=%d K=%d", M, N, K);
+  if (K % 256 != 0) return fgf8::set_error(FGF8_ERR_UNSUPPORTED, "gemm_fp4_blockscaled: K=%d not a multiple of 256", K);
+  if (N % 32 != 0) return fgf8::set_error(FGF8_ERR_UNSUPPORTED, "gemm_fp4_blockscaled: N=%d not a multiple of 32", N);
+  if (fmt != FGF8_FP4_MX && fmt != FGF8_FP4_NV)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp4_blockscaled: bad format %d", fmt);
+  if (M == 0) return FGF8_OK;
+  if (!Aq || !SFA || !Bq || !SFB || !D)
+    return fgf8::set_error(FGF8_ERR_INVALID_ARG, "gemm_fp4_blockscaled: null pointer");
+  if (!aligned16(Aq) || !aligned16(SFA) || !aligned16(Bq) || !aligned16(SFB) || !aligned16(D))
+    return fgf8::set_error(FGF8_ERR_MISALIGNED, "gemm_fp4_blockscaled: pointers must be 16-byte aligned");
+  if (int r = check_on_device("gemm_fp4_blockscaled", {Aq, SFA, Bq, SFB, D})) return r;
+  fgf8::GemmArgs a;
+  if (prepare_args(a, M, N, K, 1, D) != FGF8_OK) return FGF8_ERR_CUDA;
+  return fgf8::launch_gemm_fp4(a, Aq, SFA, Bq, SFB, fmt, static_cast<cudaStream_t>(stream));
 }
 
 int grouped_fp8_contiguous(const void* Aq, const void* SFA, const void* Bq, const void* SFB,

@@ -33,6 +33,17 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t n, uint32_t m, uint32
          | (a_sf_id << 29);   // a_sf_id
 }
 
+// 4-bit block-scaled (kind::mxf4nvf4): E2M1 A and B (format code 1), scale
+// format bit 23 (1 = E8M0 for MXFP4, 0 = E4M3 for NVFP4); the sf ids are ORed in
+// per instruction (b_sf_id bits 4-5, a_sf_id bits 29-30).
+__host__ __device__ constexpr uint32_t idesc_fp4(uint32_t n, uint32_t m, bool e8m0_scales) {
+  return (1u << 7)                        // a_format E2M1
+         | (1u << 10)                     // b_format E2M1
+         | ((n >> 3) << 17)               // n_dim
+         | ((e8m0_scales ? 1u : 0u) << 23)  // scale_format
+         | ((m >> 4) << 24);              // m_dim
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory matrix descriptor (same page, section 3.4): start address,
 // leading and stride byte offsets in 16-byte units, version 1 at bits 46-47,

@@ -17,7 +17,7 @@
 #ifndef __CUDACC_RTC__
 namespace fgf8 {
 
-enum class Kind : int { F16 = 0, MXF8 = 1, F8F32 = 2 };
+enum class Kind : int { F16 = 0, MXF8 = 1, F8F32 = 2, MXF4 = 3, NVF4 = 4 };
 enum class Sched : int { Dense = 0, Contiguous = 1, Masked = 2 };
 
 // Everything a GEMM launch needs besides the tensor maps.
@@ -71,10 +71,13 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
                      const void* Bq, const void* SFB, cudaStream_t stream);
 int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void* Bq,
                       cudaStream_t stream);
+int launch_gemm_fp4(const GemmArgs& a, const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                    int fmt, cudaStream_t stream);
 int launch_quantize_1x128(const void* X, void* Xq, void* SF, int M, int K, int fmt,
                           cudaStream_t stream);
 int launch_quantize_128x128(const void* W, void* Wq, void* SF, int G, int N, int K, int fmt,
                             cudaStream_t stream);
+int launch_quantize_fp4(const void* X, void* Xq, void* SF, int R, int K, int fmt, cudaStream_t stream);
 
 }  // namespace fgf8
 #endif

@@ -122,7 +122,11 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  set_last_tile(KIND == Kind::F16 ? "f16" : KIND == Kind::MXF8 ? "mxf8" : "f8f32",
+  set_last_tile(KIND == Kind::F16    ? "f16"
+                : KIND == Kind::MXF8 ? "mxf8"
+                : KIND == Kind::MXF4 ? "mxf4"
+                : KIND == Kind::NVF4 ? "nvf4"
+                                     : "f8f32",
                 SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, a);
   if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));

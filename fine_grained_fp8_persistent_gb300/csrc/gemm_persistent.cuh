@@ -151,7 +151,43 @@ __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
 template <int NCTA, Kind KIND>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
                                        uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  if constexpr (NCTA == 2) {
+  if constexpr (KIND == Kind::MXF4 || KIND == Kind::NVF4) {
+    // E2M1 operands packed two per byte along K, 64 elements (32 bytes) per
+    // instruction; two E8M0 (MXFP4) or four E4M3 (NVFP4) scale bytes per row and
+    // instruction, read from TMEM starting at the byte the idesc ids select
+    // ("GPU GEMM part 4: tcgen05 & Blackwell", sections 3.5 and 6.2-6.3)
+    if constexpr (NCTA == 2) {
+      if constexpr (KIND == Kind::MXF4)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+      else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+    } else {
+      if constexpr (KIND == Kind::MXF4)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+      else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+            : "memory");
+    }
+  } else if constexpr (NCTA == 2) {
     if constexpr (KIND == Kind::MXF8)
       asm volatile(
           "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
@@ -237,8 +273,16 @@ struct PCfg {
   static_assert(KIND != Kind::F8F32 || BN % 64 == 0, "promotion halves of whole 32-column chunks");
   static_assert(BN_LOCAL % 16 == 0, "B rows per CTA");
   static constexpr bool kMX = KIND == Kind::MXF8;
+  // 4-bit E2M1 operands with MXFP4 or NVFP4 block scales
+  static constexpr bool kFP4 = KIND == Kind::MXF4 || KIND == Kind::NVF4;
+  // block-scaled MMA: scale factors staged into TMEM by the writer warps
+  static constexpr bool kBS = kMX || kFP4;
   static constexpr bool kF32S = KIND == Kind::F8F32;
+  // TMA x step per K block, in elements of the operand tensor map (bytes for the
+  // 8-bit and packed 4-bit operands): every K block is 128 bytes of each row
   static constexpr int BK = (KIND == Kind::F16) ? 64 : 128;
+  // K elements per K block: 64 (16-bit), 128 (8-bit), 256 (4-bit, two per byte)
+  static constexpr int KB_ELEMS = (KIND == Kind::F16) ? 64 : kFP4 ? 256 : 128;
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
   // Rows of A staged per K block.  A thin tile (64 rows, for a dense GEMM with at
@@ -261,7 +305,15 @@ struct PCfg {
   static constexpr int KPU = AROWS_ < BM ? 4 : kF32S ? (NACC_ >= 4 ? 2 : 1) : 2;
   static_assert(STAGES % KPU == 0, "stages per unit");
   static constexpr int UNITS = STAGES / KPU;
-  static constexpr int SF_WARPS = kMX ? 4 : 0;
+  static constexpr int SF_WARPS = kBS ? 4 : 0;
+  // Scale-word groups.  A packed word holds four scale bytes of a row.  UE8M0
+  // FP8: one word per four K blocks (byte kb % 4 per K block), so a group is
+  // four K blocks.  4-bit: a K block of 256 elements needs 2 (MXFP4, 8 scales of
+  // 32) or 4 (NVFP4, 16 scales of 16) words per row, so a group is one pipeline
+  // unit.  WG: words per row per group.
+  static constexpr int GK = kFP4 ? KPU : 4;
+  static constexpr int WPK = KIND == Kind::MXF4 ? 2 : KIND == Kind::NVF4 ? 4 : 0;
+  static constexpr int WG = kFP4 ? GK * WPK : 1;
   // FP32 scales: 8 promotion warps.  A single accumulator buffer (NACC = 1,
   // 256-wide block-scaled tiles) is drained by 8 epilogue warps, two per TMEM
   // lane quarter, so that the MMAs of the next tile wait only for the drain.
@@ -289,8 +341,8 @@ struct PCfg {
                 "output quantization: whole 1x128 groups per epilogue thread");
   static_assert(!kF32S || (NACC % KPU == 0 && NSLOT >= 2), "two slots of partial buffers");
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
-  static constexpr int SFA_RING_BYTES = kMX ? BM * 4 : 0;
-  static constexpr int SFB_RING_BYTES = kMX ? SFB_ROWS * 4 : 0;
+  static constexpr int SFA_RING_BYTES = kBS ? WG * BM * 4 : 0;
+  static constexpr int SFB_RING_BYTES = kBS ? WG * SFB_ROWS * 4 : 0;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -302,7 +354,8 @@ struct PCfg {
   static constexpr int BAR_ACC_EMPTY = BAR_ACC_FULL + NACC;       // NACC
   // TMEM scale slots: three where they fit next to the accumulators, so the
   // scale writers can run two groups of K blocks ahead of the MMA
-  static constexpr int SF_SLOT_COLS = 4 + SFB_ROWS / 32;
+  static constexpr int NB_COLS = SFB_ROWS / 32;               // TMEM columns of one SFB word
+  static constexpr int SF_SLOT_COLS = WG * (4 + NB_COLS);
   static constexpr int SF_SLOTS = (NACC_ * BN + 3 * SF_SLOT_COLS <= 512) ? 3 : 2;
   static constexpr int BAR_SFR = BAR_ACC_EMPTY + NACC;            // SF_SLOTS: slot written (even CTA)
   static constexpr int BAR_SF_FREE = BAR_SFR + SF_SLOTS;          // SF_SLOTS: slot read (each CTA)
@@ -324,7 +377,7 @@ struct PCfg {
 
   static constexpr int ACC_COLS = NACC * BN;
   static constexpr int SF_COL0 = ACC_COLS;
-  static constexpr int TMEM_USED = ACC_COLS + (kMX ? SF_SLOTS * SF_SLOT_COLS : 0);
+  static constexpr int TMEM_USED = ACC_COLS + (kBS ? SF_SLOTS * SF_SLOT_COLS : 0);
   static constexpr int TMEM_ALLOC = TMEM_USED <= 32    ? 32
                                     : TMEM_USED <= 64  ? 64
                                     : TMEM_USED <= 128 ? 128
@@ -332,9 +385,11 @@ struct PCfg {
                                                        : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
-  static_assert(kF32S ? NACC >= 2 : (NACC == 2 || (NACC == 1 && BN == 256 && KIND == Kind::MXF8)),
+  static_assert(kF32S ? NACC >= 2 : (NACC == 2 || (NACC == 1 && BN == 256 && kBS)),
                 "accumulator buffers");
-  static constexpr uint32_t SF_TX = BM * 4 + BN * 4;                // bytes landing on `sf_loaded`
+  static constexpr uint32_t SF_TX = WG * (BM * 4 + BN * 4);         // bytes landing on `sf_loaded`
+  static_assert(!kFP4 || (SCHED == Sched::Dense && !QOUT_ && AROWS_ == BM && BN % 32 == 0 && KPU == GK),
+                "4-bit: dense tiles, one scale group per pipeline unit");
 };
 
 // Named-barrier rendezvous of `nthreads` threads (whole warps).  It goes through the
@@ -509,10 +564,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
   int* prefix = reinterpret_cast<int*>(smem + C::OFF_PREFIX);
 
   const int M = args.M, N = args.N, K = args.K, G = args.G;
-  const int nkb = (K + C::BK - 1) / C::BK;
+  const int nkb = (K + C::KB_ELEMS - 1) / C::KB_ELEMS;
   const int num_n = (N + BN - 1) / BN;
   const int num_m = (M + C::TILE_M - 1) / C::TILE_M;   // per expert for masked
-  const int kq = (K / 128 + 3) / 4;
+  // scale words per row of a scale table
+  const int kq = C::kFP4 ? nkb * C::WPK : (K / 128 + 3) / 4;
   const int cluster_id = static_cast<int>(blockIdx.x) / C::CLUSTER;
   const int num_clusters = static_cast<int>(gridDim.x) / C::CLUSTER;
 
@@ -526,7 +582,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       ptx::mbar_init(bar(C::BAR_ACC_FULL + b), 1);
       ptx::mbar_init(bar(C::BAR_ACC_EMPTY + b), NCTA * C::EPI_WARPS);
     }
-    if constexpr (C::kMX) {
+    if constexpr (C::kBS) {
       for (int b = 0; b < C::SF_SLOTS; ++b) {
         ptx::mbar_init(bar(C::BAR_SFR + b), NCTA * C::SF_WARPS);
         ptx::mbar_init(bar(C::BAR_SF_FREE + b), 1);
@@ -745,7 +801,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       int acc = 0;
       uint32_t gctr = 0u;            // scale-word groups consumed so far (all tiles)
       const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
-      const uint32_t idesc0 = C::kMX ? idesc_mxf8(BN, C::TILE_M, 0, 0) : idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
+      const uint32_t idesc0 = C::kMX    ? idesc_mxf8(BN, C::TILE_M, 0, 0)
+                              : C::kFP4 ? idesc_fp4(BN, C::TILE_M, KIND == Kind::MXF4)
+                                        : idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
       // descriptors are linear in the address (start field = address >> 4)
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
@@ -758,10 +816,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
           ptx::tc_fence_after();
           const int nk = min(C::KPU, nkb - kb0);
           const int kl = kb0 + nk - 1;                   // last K block of the unit
-          const bool group_end = C::kMX && (kl % 4 == 3 || kl == nkb - 1);
+          const bool group_end = C::kBS && ((kl + 1) % C::GK == 0 || kl == nkb - 1);
           if (lane == 0) {
-            if constexpr (C::kMX) {
-              if (kb0 % 4 == 0) sf_col = tmem_base + C::SF_COL0 + (gctr % C::SF_SLOTS) * C::SF_SLOT_COLS;
+            if constexpr (C::kBS) {
+              if (kb0 % C::GK == 0) sf_col = tmem_base + C::SF_COL0 + (gctr % C::SF_SLOTS) * C::SF_SLOT_COLS;
             }
 #pragma unroll
             for (int j = 0; j < C::KPU; ++j) {
@@ -774,14 +832,24 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
                 const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
                 const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
                 const uint64_t bd = bdesc0 + stage * (C::B_BYTES >> 4);
-                // block-scaled: byte kb % 4 of each scale word (a_sf_id, b_sf_id)
+                // UE8M0 FP8: byte kb % 4 of the group's scale word (a_sf_id, b_sf_id)
                 const uint32_t sfid = static_cast<uint32_t>(kb & 3);
                 const uint32_t id = C::kMX ? (idesc0 | (sfid << 4) | (sfid << 29)) : idesc0;
 #pragma unroll
                 for (int k = 0; k < C::MMAS_PER_STAGE; ++k) {
                   const uint32_t accum = C::kF32S ? (k > 0 ? 1u : 0u) : ((kb > 0 || k > 0) ? 1u : 0u);
-                  tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), id,
-                                     sf_col, sf_col + 4, accum);
+                  uint32_t sfa = sf_col, sfb = sf_col + 4, idk = id;
+                  if constexpr (C::kFP4) {
+                    // word wi of the group: MXFP4 two instructions per word (bytes
+                    // 0-1, then 2-3), NVFP4 one word per instruction (bytes 0-3)
+                    const int wi = j * C::WPK + (KIND == Kind::MXF4 ? k / 2 : k);
+                    const uint32_t fid = KIND == Kind::MXF4 ? 2u * static_cast<uint32_t>(k & 1) : 0u;
+                    sfa = sf_col + 4u * wi;
+                    sfb = sf_col + 4u * C::WG + static_cast<uint32_t>(C::NB_COLS * wi);
+                    idk = idesc0 | (fid << 4) | (fid << 29);
+                  }
+                  tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), idk,
+                                     sfa, sfb, accum);
                 }
               }
             }
@@ -818,11 +886,12 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     }
   } else if (warp < 2 + C::SF_WARPS) {
     // ============================================================ scale-factor writers
-    if constexpr (C::kMX) {
+    if constexpr (C::kBS) {
     ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
     const uint32_t q = warp & 3u;                      // TMEM lane quarter this warp writes
     const bool loader = warp == 2;                     // lane 0 of this warp issues the loads
-    constexpr int NB_COLS = C::SFB_ROWS / 32;
+    constexpr int NB_COLS = C::NB_COLS;
+    constexpr int WG = C::WG;
     if (loader && lane == 0) {
       ptx::prefetch_tmap(&tm_sfa);
       ptx::prefetch_tmap(&tm_sfb);
@@ -834,7 +903,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     };
     struct Pos { int t, kb; Tile tl; };
     auto advance = [&](Pos& p) {
-      p.kb += 4;
+      p.kb += C::GK;
       if (p.kb >= nkb) {
         p.kb = 0;
         p.t = next_valid(p.t + num_clusters, p.tl);
@@ -853,10 +922,12 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       if (lane == 0) {
         const uint32_t sfl = bar(C::BAR_SFL + r);
         ptx::mbar_arrive_expect_tx(sfl, C::SF_TX);
-        const int sfa_row = (SCHED == Sched::Masked ? pl.tl.group * kq : 0) + pl.kb / 4;
+        // the group's WG words of every row (box: rows x WG words)
+        const int w0 = pl.kb / C::GK * WG;
+        const int sfa_row = (SCHED == Sched::Masked ? pl.tl.group * kq : 0) + w0;
         ptx::tma_load_2d(sbase + C::OFF_SFA + r * C::SFA_RING_BYTES, &tm_sfa, sfl, pl.tl.m_blk, sfa_row);
         ptx::tma_load_2d(sbase + C::OFF_SFB + r * C::SFB_RING_BYTES, &tm_sfb, sfl, pl.tl.n_blk * BN,
-                         pl.tl.group * kq + pl.kb / 4);
+                         pl.tl.group * kq + w0);
       }
       __syncwarp();
       ++gl;
@@ -874,14 +945,19 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       if (loader && pl.t < num_tiles && !issue_load()) { ok = false; break; }
       const uint32_t r = gctr % C::SF_RING;
       if (!pwait(bar(C::BAR_SFL + r), (gctr / C::SF_RING) & 1u, ctl)) { ok = false; break; }
-      // word of row 32 j + l -> lane l, column j (rows past the tile are never read)
+      // word w of row 32 j + l -> lane l, column 4 w + j (SFA) or 4 WG + NB_COLS w + j
+      // (SFB); the ring slot holds the words as [w][rows] (BM rows of A, BN of B;
+      // rows past the tile are never read by the MMA)
       const uint32_t* sfa_s = reinterpret_cast<const uint32_t*>(smem + C::OFF_SFA + r * C::SFA_RING_BYTES);
       const uint32_t* sfb_s = reinterpret_cast<const uint32_t*>(smem + C::OFF_SFB + r * C::SFB_RING_BYTES);
-      uint32_t a[4], b[NB_COLS];
+      uint32_t a[WG][4], b[WG][NB_COLS];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) a[j] = sfa_s[32 * j + lane];
+      for (int w = 0; w < WG; ++w) {
 #pragma unroll
-      for (int j = 0; j < NB_COLS; ++j) b[j] = sfb_s[32 * j + lane];
+        for (int j = 0; j < 4; ++j) a[w][j] = sfa_s[w * C::BM + 32 * j + lane];
+#pragma unroll
+        for (int j = 0; j < NB_COLS; ++j) b[w][j] = sfb_s[w * BN + 32 * j + lane];
+      }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::BAR_SFC + r));
       const uint32_t slot = gctr % C::SF_SLOTS;
@@ -890,9 +966,13 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       if (uses > 0 && !pwait(bar(C::BAR_SF_FREE + slot), (uses - 1u) & 1u, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + C::SF_COL0 + slot * C::SF_SLOT_COLS;
-      tmem_st_x4(taddr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int j = 0; j < NB_COLS; j += 4) tmem_st_x4(taddr + 4 + j, b[j], b[j + 1], b[j + 2], b[j + 3]);
+      for (int w = 0; w < WG; ++w) {
+        tmem_st_x4(taddr + 4 * w, a[w][0], a[w][1], a[w][2], a[w][3]);
+#pragma unroll
+        for (int j = 0; j < NB_COLS; j += 4)
+          tmem_st_x4(taddr + 4 * WG + NB_COLS * w + j, b[w][j], b[w][j + 1], b[w][j + 2], b[w][j + 3]);
+      }
       tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -930,14 +1010,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
             if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
             if (++acc == C::NSLOT) { acc = 0; acc_phase ^= 1u; }
           }
-          if constexpr (C::kMX) {
-            if (ok && kb0 % 4 == 0)
+          if constexpr (C::kBS) {
+            if (ok && kb0 % C::GK == 0)
               ok = pwait(bar(C::BAR_SFR + gctr % C::SF_SLOTS), (gctr / C::SF_SLOTS) & 1u, ctl);
           }
           if (ok) ok = pwait(bar(C::BAR_FULL + unit), phase, ctl);
           named_bar_sync(C::HANDOFF_BAR, 64);
           const int kl = kb0 + nk - 1;
-          if (C::kMX && (kl % 4 == 3 || kl == nkb - 1)) ++gctr;
+          if (C::kBS && ((kl + 1) % C::GK == 0 || kl == nkb - 1)) ++gctr;
           if (++unit == C::UNITS) { unit = 0; phase ^= 1u; }
         }
         if constexpr (!C::kF32S) {

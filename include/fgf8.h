@@ -79,6 +79,9 @@ typedef enum {
 
 typedef enum { FGF8_F16 = 0, FGF8_BF16 = 1 } fgf8_dtype;
 typedef enum { FGF8_SCALE_F32 = 0, FGF8_SCALE_UE8M0 = 1 } fgf8_scale_fmt;
+/* 4-bit block-scaled formats ([TC5] section 6.3): E2M1 elements with an E8M0
+ * scale per 32 elements along K (MXFP4) or an E4M3 scale per 16 (NVFP4). */
+typedef enum { FGF8_FP4_MX = 0, FGF8_FP4_NV = 1 } fgf8_fp4_fmt;
 
 /*
  * quantize_1x128 -- activation quantization, 1x128 groups ([DG] "fine-grained
@@ -177,6 +180,41 @@ FGF8_API int grouped_fp8_contiguous(const void* Aq, const void* SFA, const void*
 FGF8_API int grouped_fp8_masked(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
                        const int32_t* masked_m, void* D, int G, int Mmax, int N, int K,
                        int expected_m, int fmt, void* stream);
+
+/*
+ * quantize_fp4 -- 4-bit block quantization of the rows of X along K, for either
+ * GEMM operand ([TC5] section 6.1: every SV consecutive K elements of a row
+ * share one scale; section 6.3: SV = 32 with an E8M0 scale for MXFP4, SV = 16
+ * with an E4M3 scale for NVFP4; section 7.1: two elements per byte along K).
+ *   X  : bf16 [R][K]               input
+ *   Xq : uint8 [R][K/2]            E2M1 codes, element 2j in the low nibble of
+ *                                  byte j, element 2j+1 in the high nibble (output)
+ *   SF : int32 [ceil(K/SV/4)][align4(R)] (output): byte j of word (w, r) is the
+ *        scale of group 4w+j of row r; unused bytes and rows R..align4(R)-1 are 0.
+ * MXFP4 scale 2^e, e = ceil(log2(amax/6)) (FP32 quotient) clamped to
+ * [-127, 127], stored as e + 127, codes E2M1(x * 2^-e).  NVFP4 scale
+ * s = E4M3(amax/6) (nearest even, saturating), codes E2M1(x / s) (FP32
+ * division; all codes 0 when s is 0).  An all-zero group has scale 1.  E2M1
+ * rounds to nearest even and saturates at +-6.
+ * Requires K % 64 == 0, R >= 0; fmt is an fgf8_fp4_fmt.
+ */
+FGF8_API int quantize_fp4(const void* X, void* Xq, void* SF, int R, int K, int fmt, void* stream);
+
+/*
+ * gemm_fp4_blockscaled -- dense 4-bit block-scaled NT GEMM ([TC5] section 6.1):
+ *   D[m,n] = sum_k (A[m,k] * SFA[m, k/SV]) * (B[n,k] * SFB[n, k/SV])
+ * on the block-scaled tensor-core MMA (kind::mxf4nvf4, scale_vec 2X for MXFP4,
+ * 4X for NVFP4), FP32 accumulation, bf16 output.
+ *   Aq : uint8 [M][K/2], SFA : scale table of M rows (quantize_fp4 layouts)
+ *   Bq : uint8 [N][K/2], SFB : scale table of N rows
+ *   D  : bf16 [M][N]
+ * Requires K % 256 == 0, N % 32 == 0, M >= 0.
+ */
+FGF8_API int gemm_fp4_blockscaled(const void* Aq, const void* SFA, const void* Bq, const void* SFB,
+                                  void* D, int M, int N, int K, int fmt, void* stream);
+
+/* Bytes of a quantize_fp4 scale table for R rows; -1 on invalid arguments. */
+FGF8_API long long fgf8_fp4_sf_bytes(int R, int K, int fmt);
 
 /* Row alignment of expert segments in the contiguous layout (the BLOCK_M of the
  * kernel; [DG] mentions a query of this name for the contiguous layout). */

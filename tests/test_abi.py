@@ -84,6 +84,29 @@ def test_host_validation(lib):
     assert q(None, None, None, None, None, None, 0, 256, 256, 1, 1, None) == 0
 
 
+def test_host_validation_fp4(lib):
+    P = ctypes.c_void_p
+    al = P(0x10000)
+    q = lib.quantize_fp4
+    q.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    assert q(al, al, al, 4, 96, 0, None) == 2 and "multiple of 64" in _err(lib)
+    assert q(al, al, al, 4, 128, 2, None) == 1
+    assert q(al, al, al, -1, 128, 0, None) == 1
+    assert q(None, None, None, 0, 128, 1, None) == 0
+    g = lib.gemm_fp4_blockscaled
+    g.argtypes = [P] * 5 + [ctypes.c_int] * 4 + [P]
+    assert g(al, al, al, al, al, 16, 64, 128, 0, None) == 2 and "multiple of 256" in _err(lib)
+    assert g(al, al, al, al, al, 16, 48, 256, 0, None) == 2 and "multiple of 32" in _err(lib)
+    assert g(al, al, al, al, al, 16, 64, 256, 3, None) == 1
+    assert g(al, P(0x10004), al, al, al, 16, 64, 256, 1, None) == 3
+    assert g(None, None, None, None, None, 0, 64, 256, 1, None) == 0
+    lib.fgf8_fp4_sf_bytes.restype = ctypes.c_longlong
+    assert lib.fgf8_fp4_sf_bytes(4096, 7168, 0) == 56 * 4096 * 4      # 224 groups of 32
+    assert lib.fgf8_fp4_sf_bytes(37, 7168, 1) == 112 * 40 * 4         # 448 groups of 16
+    assert lib.fgf8_fp4_sf_bytes(8, 64, 0) == 1 * 8 * 4               # 2 groups: half a word
+    assert lib.fgf8_fp4_sf_bytes(8, 100, 0) == -1
+
+
 def test_size_helpers(lib):
     lib.fgf8_sfa_bytes.restype = ctypes.c_longlong
     lib.fgf8_sfb_bytes.restype = ctypes.c_longlong
