@@ -958,6 +958,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
 #pragma unroll
         for (int j = 0; j < NB_COLS; ++j) b[w][j] = sfb_s[w * BN + 32 * j + lane];
       }
+      // The slot is refilled by TMA, an async-proxy write: each lane orders its
+      // generic-proxy reads of the slot before that write with a proxy fence
+      // (without it the refill of the next round was seen by late readers, so a
+      // lane quarter applied the scales of a group four groups ahead).
+      ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::BAR_SFC + r));
       const uint32_t slot = gctr % C::SF_SLOTS;

@@ -113,6 +113,23 @@ def test_fp4_gemm_full_size(fg, dev, oracle, fmt):
     gemm_close(got[r, c], loop, f"fp4 full fmt{fmt} (triple loop)")
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+def test_fp4_gemm_full_size_repeated_pair_tiles(fg, dev, oracle, monkeypatch, fmt):
+    """The CTA-pair tiles at full size, several launches each, every element
+    against the oracle: a late reader of the scale-word ring that sees the slot's
+    next group shows up as outlier-sized errors in one lane quarter of a few
+    tiles, in some launches only."""
+    M = 4096
+    N = K = 7168
+    case = _fp4_case(M, N, K, fmt, 11)
+    ref = oracle.gemm_fp4_dequant(*case, fmt)
+    for tile in ("2x256", "2x128"):
+        monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+        for rep in range(3):
+            out = _run(fg, dev, case, fmt, M, N)
+            gemm_close(out.float().cpu().numpy(), ref, f"fp4 full fmt{fmt} {tile} launch {rep}")
+
+
 def _row_sf(oracle, sf, row, R, K, fmt):
     """The scale table of one row, cut out of an R-row table."""
     shape, dt = oracle.fp4_sf_shape(1, K, fmt)

@@ -70,6 +70,22 @@ def test_fp8_dense_full_size(fg, dev, oracle, fmt, M):
     gemm_close(got[r, c], oracle.gemm_fp8_entries(*case, fmt, r, c), f"fp8 full M={M} fmt{fmt} (triple loop)")
 
 
+def test_ue8m0_full_size_repeated_pair_tiles(fg, dev, oracle, monkeypatch):
+    """UE8M0 scales at 4096 x 7168 x 7168 on the CTA-pair tiles, several launches
+    each, every element against the oracle (the scale words pass through the same
+    TMA-filled ring as the 4-bit kernels', whose late readers once saw the slot's
+    next group)."""
+    M = 4096
+    N = K = 7168
+    case = _fp8_case(M, N, K, 1, 7)
+    ref = oracle.gemm_fp8_dequant(*case, 1)
+    for tile in ("2x256", "2x224", "2x128"):
+        monkeypatch.setenv("FGF8_FORCE_TILE", tile)
+        for rep in range(2):
+            out = _run_fp8(fg, dev, case, 1, M, N)
+            gemm_close(out.float().cpu().numpy(), ref, f"ue8m0 full {tile} launch {rep}")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_fp8_deterministic(fg, dev, fmt):
     case = _fp8_case(256, 512, 1024, fmt, 5)
