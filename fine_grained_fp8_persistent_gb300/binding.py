@@ -64,6 +64,9 @@ _SIGS = {
     "fgf8_set_wait_timeout_ms": ([_I], _I),
     "fgf8_selftest_wait_timeout": ([_P], _I),
     "fgf8_set_pdl": ([_I], _I),
+    "fgf8_set_scheduler": ([_I], _I),
+    "fgf8_set_sm_cap": ([_I], _I),
+    "fgf8_persistent_clusters": ([_LL, _I, _I, _I, _I], _LL),
     "fgf8_version": ([], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -406,6 +409,27 @@ def selftest_wait_timeout(stream=None) -> None:
 def set_pdl(enable: bool) -> bool:
     """Turn programmatic dependent launch on or off; returns the previous setting."""
     return bool(_lib.fgf8_set_pdl(1 if enable else 0))
+
+
+SCHED_STATIC = 0
+SCHED_CLC = 1
+
+
+def set_scheduler(mode: int) -> int:
+    """Tile scheduler of the GEMMs: SCHED_STATIC (persistent grid, static round
+    robin) or SCHED_CLC (one cluster per tile, cluster launch control hands out the
+    tiles of clusters not yet launched); returns the previous mode."""
+    return int(_lib.fgf8_set_scheduler(int(mode)))
+
+
+def set_sm_cap(enable: bool) -> bool:
+    """Wave-preserving SM cap of the static persistent grid; returns the previous setting."""
+    return bool(_lib.fgf8_set_sm_cap(1 if enable else 0))
+
+
+def persistent_clusters(tiles: int, cluster: int, sms: int, max_clusters: int, cap: bool) -> int:
+    """Clusters of the static persistent grid the launcher picks (host arithmetic)."""
+    return int(_lib.fgf8_persistent_clusters(int(tiles), int(cluster), int(sms), int(max_clusters), 1 if cap else 0))
 
 
 def set_wait_timeout_ms(ms: int) -> int:

@@ -23,6 +23,8 @@ __device__ uint32_t g_status;
 
 thread_local char g_errbuf[512];
 int g_pdl = -1;   // -1 = not read from the environment yet
+int g_sched = -1;  // tile scheduler; -1 = not read from the environment yet
+int g_smcap = -1;  // wave-preserving SM cap of persistent grids; -1 = not read yet
 thread_local char g_last_tile[64];
 
 struct DevInfo {
@@ -110,6 +112,37 @@ bool pdl_enabled() {
     g_pdl = (e != nullptr && e[0] == '0') ? 0 : 1;
   }
   return g_pdl != 0;
+}
+
+int scheduler_mode() {
+  if (g_sched < 0) {
+    const char* e = std::getenv("FGF8_SCHED");
+    g_sched = (e != nullptr && std::strcmp(e, "clc") == 0) ? 1 : 0;
+  }
+  return g_sched;
+}
+
+bool sm_cap_enabled() {
+  if (g_smcap < 0) {
+    const char* e = std::getenv("FGF8_SM_CAP");
+    g_smcap = (e != nullptr && e[0] == '0') ? 0 : 1;
+  }
+  return g_smcap != 0;
+}
+
+// "DeepGEMM dissected", section on the SM count (num_min_sms): the fewest SMs that
+// keep the number of waves, but never fewer than all SMs but 8, in whole clusters.
+long long persistent_clusters(long long tiles, int cluster, int sms, int max_clusters, bool cap) {
+  if (tiles < 1 || cluster < 1 || max_clusters < 1) return 1;
+  long long clusters = tiles < max_clusters ? tiles : max_clusters;
+  if (!cap) return clusters;
+  const long long waves = (tiles + clusters - 1) / clusters;
+  const long long wave_sms = (tiles + waves - 1) / waves * cluster;
+  const long long floor_sms = sms - 8;
+  const long long want_sms = wave_sms > floor_sms ? wave_sms : floor_sms;
+  long long c = (want_sms + cluster - 1) / cluster;
+  if (c > clusters) c = clusters;
+  return c < 1 ? 1 : c;
 }
 
 int set_error(int code, const char* fmt, ...) {
@@ -206,6 +239,22 @@ int fgf8_set_pdl(int enable) {
   const int prev = fgf8::pdl_enabled() ? 1 : 0;
   if (enable == 0 || enable == 1) g_pdl = enable;
   return prev;
+}
+
+int fgf8_set_scheduler(int mode) {
+  const int prev = fgf8::scheduler_mode();
+  if (mode == 0 || mode == 1) g_sched = mode;
+  return prev;
+}
+
+int fgf8_set_sm_cap(int enable) {
+  const int prev = fgf8::sm_cap_enabled() ? 1 : 0;
+  if (enable == 0 || enable == 1) g_smcap = enable;
+  return prev;
+}
+
+long long fgf8_persistent_clusters(long long tiles, int cluster, int sms, int max_clusters, int cap) {
+  return fgf8::persistent_clusters(tiles, cluster, sms, max_clusters, cap != 0);
 }
 
 int fgf8_set_wait_timeout_ms(int ms) {

@@ -43,6 +43,10 @@ struct GemmArgs {
   uint8_t* dq;
   void* sfd;
   int dq_ue8m0;               // 1: UE8M0 scales, 0: FP32 scales
+  // Tile scheduling: 0 = static round robin over a persistent grid; 1 = cluster
+  // launch control (a grid of one cluster per tile; running clusters cancel the
+  // clusters not yet launched and take their tiles)
+  int clc;
 };
 
 struct TensorMaps {
@@ -53,6 +57,14 @@ struct TensorMaps {
 int set_error(int code, const char* fmt, ...);
 // Whether kernels are launched with programmatic stream serialization (PDL).
 bool pdl_enabled();
+// Tile scheduler of the GEMMs (0 static, 1 cluster launch control) and whether
+// the persistent grid is capped by the wave-preserving SM count.
+int scheduler_mode();
+bool sm_cap_enabled();
+// Clusters of a static persistent grid for `tiles` cluster tiles: at most
+// max_clusters; with the cap, the fewest that keep the number of waves, but not
+// fewer than (sms - 8) SMs' worth, rounded to whole clusters.
+long long persistent_clusters(long long tiles, int cluster, int sms, int max_clusters, bool cap);
 // Launches the bounded-wait self-test (selftest.cu).
 int launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // Records the configuration of the GEMM launch this thread makes (fgf8_last_tile).

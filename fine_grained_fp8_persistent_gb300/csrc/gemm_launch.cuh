@@ -118,8 +118,22 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
       return set_error(4, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
     max_clusters[dev] = clusters;
   }
-  long long clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
-  if (clusters < 1) clusters = 1;
+  // static schedule: a persistent grid, capped for dense GEMMs by the wave-preserving
+  // SM count (grouped layouts only know an upper bound of their tiles here); cluster
+  // launch control: one cluster per tile, the kernel cancels the clusters that have
+  // not launched yet and takes their tiles
+  GemmArgs la = a;
+  la.clc = scheduler_mode();
+  long long clc_tiles = tiles;
+  if (SCHED == Sched::Contiguous && CL == 2) {
+    // pairs are cut per run of same-expert blocks on the device: at most one pair
+    // tile per 128-row block, whatever the runs (a bound that holds for any m_indices)
+    clc_tiles = static_cast<long long>((a.M + 127) / 128) * ((a.N + BN - 1) / BN);
+  }
+  long long clusters = la.clc ? (clc_tiles > 0 ? clc_tiles : 1)
+                              : persistent_clusters(tiles, CL, device_sm_count(), max_clusters[dev],
+                                                    SCHED == Sched::Dense && sm_cap_enabled());
+  if (clusters * CL > 0x7FFFFFFFLL) return set_error(2, "gemm launch: %lld tiles exceed the grid limit", tiles);
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   set_last_tile(KIND == Kind::F16    ? "f16"
@@ -128,7 +142,7 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
                 : KIND == Kind::NVF4 ? "nvf4"
                                      : "f8f32",
                 SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, la);
   if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
   return 0;
 }

@@ -230,6 +230,20 @@ __device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) 
   return ptx::mbar_try_wait(bar, parity);
 }
 
+// Test a phase of a barrier in this CTA with cluster-scope acquire (the barrier's
+// data was stored from another CTA of the cluster).
+__device__ __forceinline__ bool try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 struct PairWaitCtl {
   volatile uint32_t* abort_flag;   // this CTA's flag (shared memory)
   uint32_t peer_abort;             // the peer's flag (cluster address), 0 if none
@@ -238,12 +252,14 @@ struct PairWaitCtl {
   uint32_t role_bit;
 };
 
+template <bool ACQ_CLUSTER = false>
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairWaitCtl& c) {
-  bool ok = try_wait_cluster(bar, parity);
+  auto test = [&]() { return ACQ_CLUSTER ? try_wait_acq_cluster(bar, parity) : try_wait_cluster(bar, parity); };
+  bool ok = test();
   if (!ok) {
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
-      if (try_wait_cluster(bar, parity)) { ok = true; break; }
+      if (test()) { ok = true; break; }
       if ((i & 63u) == 0) {
         if (*c.abort_flag) break;
         if (ptx::globaltimer() - t0 > c.timeout_ns) {
@@ -320,7 +336,9 @@ struct PCfg {
   static constexpr int EPI_WARPS = (kF32S || NACC_ == 1) ? 8 : 4;
   static constexpr int EPI_WARP0 = 2 + SF_WARPS;
   static constexpr int RELAY_WARP = EPI_WARP0 + EPI_WARPS;
-  static constexpr int THREADS = 32 * (RELAY_WARP + 1);
+  // tile scheduler of cluster launch control (idle under the static schedule)
+  static constexpr int SCHED_WARP = RELAY_WARP + 1;
+  static constexpr int THREADS = 32 * (SCHED_WARP + 1);
   static constexpr int HANDOFF_BAR = 1;              // named barrier: relay warp + MMA warp
   static constexpr int MAX_GROUPS = 1024;
 
@@ -362,7 +380,20 @@ struct PCfg {
   static constexpr int BAR_SFL = BAR_SF_FREE + SF_SLOTS;          // SF_RING: words landed (local)
   static constexpr int BAR_SFC = BAR_SFL + SF_RING;               // SF_RING: words read (local)
   static constexpr int BAR_DRAIN = BAR_SFC + SF_RING;
-  static constexpr int NUM_BARS = BAR_DRAIN + 1;
+  // cluster launch control: the scheduler warp's try_cancel response lands in a
+  // 16-byte staging slot (BAR_CLC_STAGE, leader); the tiles it accepts are
+  // published as tile ids into a ring of CLC_Q slots in every CTA of the cluster.  A
+  // ring slot is full once its tile id is published (one arrival) and empty when
+  // every epilogue warp of the cluster has finished that tile.  The ring is
+  // deeper than any role runs ahead of the epilogue in tiles: the scale-word loader
+  // (three groups ahead of the writers, who are up to three ahead of the MMA, which
+  // is up to two tiles ahead of the epilogue) and the producer (up to UNITS units
+  // ahead of the MMA), with at least one group and one unit per tile.
+  static constexpr int CLC_Q = 12;
+  static constexpr int BAR_CLC_FULL = BAR_DRAIN + 1;              // CLC_Q (each CTA)
+  static constexpr int BAR_CLC_EMPTY = BAR_CLC_FULL + CLC_Q;      // CLC_Q (leader)
+  static constexpr int BAR_CLC_STAGE = BAR_CLC_EMPTY + CLC_Q;     // 1 (leader)
+  static constexpr int NUM_BARS = BAR_CLC_STAGE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_PREFIX = (OFF_MISC + 16 + 15) / 16 * 16;
   // contiguous layout on CTA pairs: tiles are cut per expert segment (run of
@@ -373,7 +404,9 @@ struct PCfg {
   static constexpr int PREFIX_BYTES = (SCHED == Sched::Masked) ? (MAX_GROUPS + 1) * 4
                                       : kRuns                  ? 3 * (MAX_RUNS + 1) * 4
                                                                : 0;
-  static constexpr int SMEM_BYTES = OFF_PREFIX + PREFIX_BYTES + 1024;
+  // staging response (16 bytes), then CLC_Q published tile ids (int32, -1 = end)
+  static constexpr int OFF_CLC = (OFF_PREFIX + PREFIX_BYTES + 15) / 16 * 16;
+  static constexpr int SMEM_BYTES = OFF_CLC + 16 + 4 * CLC_Q + 1024;
 
   static constexpr int ACC_COLS = NACC * BN;
   static constexpr int SF_COL0 = ACC_COLS;
@@ -391,6 +424,40 @@ struct PCfg {
   static_assert(!kFP4 || (SCHED == Sched::Dense && !QOUT_ && AROWS_ == BM && BN % 32 == 0 && KPU == GK),
                 "4-bit: dense tiles, one scale group per pipeline unit");
 };
+
+// Cluster launch control ("Dissecting NVIDIA Blackwell" (EEPW), the feature list):
+// asks the hardware to cancel one cluster of this grid that has not launched yet
+// (a pair is cancelled whole).  The 16-byte response lands at `resp` and completes
+// 16 transaction bytes on the barrier `bar`, both in this CTA.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::
+                   "r"(resp),
+               "r"(bar)
+               : "memory");
+}
+// Publishes a tile id to a CTA of the cluster: the store, then an arrive with
+// cluster-scope release on that CTA's barrier, so that a waiter there that
+// acquires at cluster scope reads the id.
+__device__ __forceinline__ void clc_publish(uint32_t slot_cluster, uint32_t bar_cluster, int tile) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(slot_cluster), "r"(tile) : "memory");
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// The cluster a response names (the x index of its first CTA over the cluster
+// size), or -1 when nothing was cancelled: every cluster has launched.
+__device__ __forceinline__ int clc_cluster(uint32_t resp, int cluster) {
+  uint32_t x, ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 cr;\n\t"
+      "ld.shared.b128 cr, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, cr;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "mov.u32 %0, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, cr;\n\t}"
+      : "=r"(x), "=r"(ok)
+      : "r"(resp)
+      : "memory");
+  return ok ? static_cast<int>(x) / cluster : -1;
+}
 
 // Named-barrier rendezvous of `nthreads` threads (whole warps).  It goes through the
 // CTA barrier unit, not shared memory: the MMA warp waits here instead of polling an
@@ -573,6 +640,17 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
   const int num_clusters = static_cast<int>(gridDim.x) / C::CLUSTER;
 
   // ---------------------------------------------------------------- set-up
+  // The tensor maps are kernel parameters, not data of the previous kernel: fetch
+  // them into the TMA unit's cache now, under the barrier and TMEM set-up (after an
+  // L2 flush the first TMA load otherwise waits a DRAM round trip for them).
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_a);
+    ptx::prefetch_tmap(&tm_b);
+    if constexpr (C::kBS) {
+      ptx::prefetch_tmap(&tm_sfa);
+      ptx::prefetch_tmap(&tm_sfb);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int u = 0; u < C::UNITS; ++u) {
       ptx::mbar_init(bar(C::BAR_FULL + u), 1);
@@ -593,6 +671,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       }
     }
     ptx::mbar_init(bar(C::BAR_DRAIN), 1);
+    for (int q = 0; q < C::CLC_Q; ++q) {
+      ptx::mbar_init(bar(C::BAR_CLC_FULL + q), 1);
+      ptx::mbar_init(bar(C::BAR_CLC_EMPTY + q), NCTA * C::EPI_WARPS);
+    }
+    ptx::mbar_init(bar(C::BAR_CLC_STAGE), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -759,19 +842,66 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
                   args.status, args.timeout_ns, 0};
   bool aborted = false;
 
+  // ---------------------------------------------------------------- tile sequence
+  // Every role walks the same sequence of tiles.  Static schedule: cluster_id,
+  // cluster_id + num_clusters, ...  Cluster launch control (args.clc): the grid has
+  // one cluster per tile; sequence index 0 is this cluster's own tile, index i >= 1
+  // the tile of the cluster that the i-th request cancelled (slot (i - 1) % CLC_Q
+  // of the response ring; requests come from the scheduler warp, and a slot is
+  // refilled only after every epilogue warp of the cluster has finished the tile
+  // it named: the epilogue is the last role to leave a tile).  Tiles past
+  // num_tiles (grouped layouts launch an upper bound) are skipped, not treated as
+  // the end.
+  constexpr int kSeqEnd = 0x7FFFFFFF;
+  struct Seq {
+    int t;
+    uint32_t i;
+  };
+  auto seq_begin = [&]() -> Seq {
+    Seq sq{cluster_id, 0u};
+    if (!args.clc && sq.t >= num_tiles) sq.t = kSeqEnd;
+    return sq;
+  };
+  auto seq_next = [&](Seq& sq) {
+    if (!args.clc) {
+      sq.t += num_clusters;
+      if (sq.t >= num_tiles) sq.t = kSeqEnd;
+      return;
+    }
+    ++sq.i;
+    const uint32_t r = sq.i - 1u;
+    if (!pwait<true>(bar(C::BAR_CLC_FULL + r % C::CLC_Q), (r / C::CLC_Q) & 1u, ctl)) {
+      sq.t = kSeqEnd;
+      return;
+    }
+    const int c = *reinterpret_cast<volatile const int*>(smem + C::OFF_CLC + 16 + 4 * (r % C::CLC_Q));
+    sq.t = c < 0 ? kSeqEnd : c;
+  };
+  // advances to the first tile at or after the cursor that this CTA works on
+  auto seq_valid = [&](Seq& sq, Tile& tl) {
+    while (sq.t != kSeqEnd && (sq.t >= num_tiles || !get_tile(sq.t, tl))) seq_next(sq);
+  };
+  // Epilogue warps, after finishing sequence index i >= 1: release its ring slot
+  // (every epilogue warp of the cluster, on the leader's barrier).
+  auto seq_step_epi = [&](Seq& sq) {
+    if (args.clc && sq.i >= 1u) {
+      const uint32_t q = (sq.i - 1u) % C::CLC_Q;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_CLC_EMPTY + q));
+      __syncwarp();
+    }
+    seq_next(sq);
+  };
+
   if (warp == 0) {
     // ============================================================ TMA producer
     ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tm_a);
-      ptx::prefetch_tmap(&tm_b);
-    }
     int unit = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+    for (Seq sq = seq_begin(); ok && sq.t != kSeqEnd; seq_next(sq)) {
       Tile tl;
-      if (!get_tile(t, tl)) continue;
+      if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
         if (!pwait(bar(C::BAR_EMPTY + unit), phase ^ 1u, ctl)) { ok = false; break; }
         if (lane == 0) {
@@ -807,9 +937,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       // descriptors are linear in the address (start field = address >> 4)
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
-      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      for (Seq sq = seq_begin(); sq.t != kSeqEnd; seq_next(sq)) {
         Tile tl;
-        if (!get_tile(t, tl)) continue;
+        if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
         uint32_t sf_col = 0;
         for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
           named_bar_sync(C::HANDOFF_BAR, 64);
@@ -892,28 +1022,21 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     const bool loader = warp == 2;                     // lane 0 of this warp issues the loads
     constexpr int NB_COLS = C::NB_COLS;
     constexpr int WG = C::WG;
-    if (loader && lane == 0) {
-      ptx::prefetch_tmap(&tm_sfa);
-      ptx::prefetch_tmap(&tm_sfb);
-    }
-    auto next_valid = [&](int t, Tile& tl) -> int {
-      for (; t < num_tiles; t += num_clusters)
-        if (get_tile(t, tl)) return t;
-      return num_tiles;
-    };
-    struct Pos { int t, kb; Tile tl; };
+    struct Pos { Seq sq; int kb; Tile tl; };
     auto advance = [&](Pos& p) {
       p.kb += C::GK;
       if (p.kb >= nkb) {
         p.kb = 0;
-        p.t = next_valid(p.t + num_clusters, p.tl);
+        seq_next(p.sq);
+        seq_valid(p.sq, p.tl);
       }
     };
     // The loader keeps SF_RING - 1 groups in flight ahead of the writers.  A ring
     // slot is reloaded once all four writers have read its previous group.
     Pos pl;
     pl.kb = 0;
-    pl.t = next_valid(cluster_id, pl.tl);
+    pl.sq = seq_begin();
+    seq_valid(pl.sq, pl.tl);
     uint32_t gl = 0;
     auto issue_load = [&]() -> bool {
       const uint32_t r = gl % C::SF_RING;
@@ -936,13 +1059,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     };
     bool ok = true;
     if (loader)
-      for (int i = 0; ok && i < C::SF_RING - 1 && pl.t < num_tiles; ++i) ok = issue_load();
+      for (int i = 0; ok && i < C::SF_RING - 1 && pl.sq.t != kSeqEnd; ++i) ok = issue_load();
     Pos pw;
     pw.kb = 0;
-    pw.t = next_valid(cluster_id, pw.tl);
+    pw.sq = seq_begin();
+    seq_valid(pw.sq, pw.tl);
     uint32_t gctr = 0;
-    while (ok && pw.t < num_tiles) {
-      if (loader && pl.t < num_tiles && !issue_load()) { ok = false; break; }
+    while (ok && pw.sq.t != kSeqEnd) {
+      if (loader && pl.sq.t != kSeqEnd && !issue_load()) { ok = false; break; }
       const uint32_t r = gctr % C::SF_RING;
       if (!pwait(bar(C::BAR_SFL + r), (gctr / C::SF_RING) & 1u, ctl)) { ok = false; break; }
       // word w of row 32 j + l -> lane l, column 4 w + j (SFA) or 4 WG + NB_COLS w + j
@@ -987,6 +1111,53 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     }
     aborted = !ok;
     }
+  } else if (warp == C::SCHED_WARP) {
+    // ============================================================ tile scheduler
+    // Cluster launch control only, leader CTA: fills the ring with the tiles of
+    // sequence indices 1, 2, ...  For each index it waits until every epilogue warp
+    // of the cluster has finished the tile the slot held, then cancels clusters one
+    // at a time (each request after the previous response has landed, so none is in
+    // flight when the CTA exits) until one names a tile this grid works on, and
+    // publishes that tile id to both CTAs; a request that finds no cluster left
+    // publishes the end.  Clusters past the tiles (grouped layouts launch an upper
+    // bound) are cancelled and dropped here, so every published tile is real work.
+    if (args.clc && leader) {
+      ctl.role_bit = FGF8_DEVERR_ROLE_PRODUCER;
+      uint32_t sphase = 0;
+      const uint32_t stage = sbase + C::OFF_CLC;
+      for (uint32_t idx = 1;; ++idx) {
+        const uint32_t q = (idx - 1u) % C::CLC_Q;
+        if (idx > static_cast<uint32_t>(C::CLC_Q)) {
+          const uint32_t prev = idx - 1u - C::CLC_Q;   // the slot's previous index is prev + 1
+          if (!pwait(bar(C::BAR_CLC_EMPTY + q), (prev / C::CLC_Q) & 1u, ctl)) break;
+        }
+        int tile = -1;
+        bool failed = false;
+        for (;;) {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::BAR_CLC_STAGE), 16u);
+            clc_try_cancel(stage, bar(C::BAR_CLC_STAGE));
+          }
+          __syncwarp();
+          if (!pwait(bar(C::BAR_CLC_STAGE), sphase, ctl)) { failed = true; break; }
+          sphase ^= 1u;
+          const int c = clc_cluster(stage, C::CLUSTER);
+          if (c < 0) break;
+          Tile tl;
+          if (c < num_tiles && get_tile(c, tl)) { tile = c; break; }
+        }
+        if (failed) break;
+        if (lane == 0) {
+          for (uint32_t rk = 0; rk < static_cast<uint32_t>(NCTA); ++rk) {
+            const uint32_t slot = sbase + C::OFF_CLC + 16u + 4u * q;
+            clc_publish(NCTA == 2 ? map_to_rank(slot, rk) : slot,
+                        NCTA == 2 ? map_to_rank(bar(C::BAR_CLC_FULL + q), rk) : bar(C::BAR_CLC_FULL + q), tile);
+          }
+        }
+        __syncwarp();
+        if (tile < 0) break;
+      }
+    }
   } else if (warp == C::RELAY_WARP) {
     // ============================================================ relay
     // Waits, for the MMA warp, on everything a unit of MMAs needs (operands landed,
@@ -1002,9 +1173,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       uint32_t acc_phase = 0;
       uint32_t gctr = 0u;
       bool ok = true;
-      for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+      for (Seq sq = seq_begin(); sq.t != kSeqEnd; seq_next(sq)) {
         Tile tl;
-        if (!get_tile(t, tl)) continue;
+        if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
         if constexpr (!C::kF32S) {
           if (ok) ok = pwait(bar(C::BAR_ACC_EMPTY + acc), acc_phase ^ 1u, ctl);
         }
@@ -1039,9 +1210,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+    for (Seq sq = seq_begin(); sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
-      if (!get_tile(t, tl)) continue;
+      if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
       const int r = static_cast<int>(q * 32 + lane);
@@ -1139,9 +1310,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+    for (Seq sq = seq_begin(); sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
-      if (!get_tile(t, tl)) continue;
+      if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
       const int r = static_cast<int>(q * 32 + lane);
@@ -1208,27 +1379,25 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     // so that nothing waits for them before the next unit: a row past the tile's
     // valid rows, or columns past N, read the table's first entries instead, and
     // those values only reach outputs that are never stored.
-    int s_t = cluster_id;
+    Seq s_sq = seq_begin();
     int s_kb0 = 0;
     const float* s_pa = args.sfa_f32;
     const float* s_pb = args.sfb_f32;
-    auto stream_seek = [&]() {  // first tile at or after s_t that this CTA works on
+    auto stream_seek = [&]() {  // first tile at or after the stream's cursor that this CTA works on
       s_pa = args.sfa_f32;
       s_pb = args.sfb_f32;
-      for (; s_t < num_tiles; s_t += num_clusters) {
-        Tile st;
-        if (!get_tile(s_t, st)) continue;
-        const int c0 = st.n_blk * BN + h * HALF;
-        if (r < st.row_limit)
-          s_pa = args.sfa_f32 + (SCHED == Sched::Masked ? static_cast<size_t>(st.group) * nkb128 * ld_a : 0) +
-                 (st.m_blk + r);
-        if (c0 < N) s_pb = args.sfb_f32 + (static_cast<size_t>(st.group) * nnb + c0 / 128) * nkb128;
-        return;
-      }
+      Tile st;
+      seq_valid(s_sq, st);
+      if (s_sq.t == kSeqEnd) return;
+      const int c0 = st.n_blk * BN + h * HALF;
+      if (r < st.row_limit)
+        s_pa = args.sfa_f32 + (SCHED == Sched::Masked ? static_cast<size_t>(st.group) * nkb128 * ld_a : 0) +
+               (st.m_blk + r);
+      if (c0 < N) s_pb = args.sfb_f32 + (static_cast<size_t>(st.group) * nnb + c0 / 128) * nkb128;
     };
     float na[C::KPU], nb[C::KPU];  // the next unit's scales, in flight
     auto stream_fetch = [&]() {
-      if (s_t < num_tiles) {
+      if (s_sq.t != kSeqEnd) {
 #pragma unroll
         for (int j = 0; j < C::KPU; ++j) {
           const int kb = min(s_kb0 + j, nkb - 1);  // a short tail unit repeats its last K block
@@ -1238,7 +1407,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         s_kb0 += C::KPU;
         if (s_kb0 >= nkb) {
           s_kb0 = 0;
-          s_t += num_clusters;
+          seq_next(s_sq);
           stream_seek();
         }
       }
@@ -1283,9 +1452,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         }
       }
     };
-    for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+    for (Seq sq = seq_begin(); ok && sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
-      if (!get_tile(t, tl)) continue;
+      if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       bool row_ok = r < tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {

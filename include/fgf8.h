@@ -263,6 +263,32 @@ FGF8_API int fgf8_selftest_wait_timeout(void* stream);
  * else leaves it unchanged.  Returns the previous setting. */
 FGF8_API int fgf8_set_pdl(int enable);
 
+/* Tile scheduler of the GEMM kernels ("Dissecting NVIDIA Blackwell" (EEPW), the
+ * feature list: cluster launch control).  0 (default; FGF8_SCHED unset): a
+ * persistent grid of at most one CTA (or CTA pair) per SM walks the tiles in a
+ * static round robin.  1 (FGF8_SCHED=clc at first use): the grid holds one
+ * cluster per tile; each running cluster, as it drains its tiles, cancels clusters
+ * that have not launched yet (clusterlaunchcontrol.try_cancel) and takes their
+ * tiles, so the work is handed out dynamically.  Results are identical either way
+ * up to the order of tiles.  mode: 0 or 1, anything else leaves it unchanged.
+ * Returns the previous mode. */
+FGF8_API int fgf8_set_scheduler(int mode);
+
+/* Wave-preserving SM cap of the static persistent grid of dense GEMMs
+ * ("DeepGEMM dissected", section on the number of SMs launched: num_min_sms =
+ * ceil(max(SMs the waves need, SMs - 8) / cluster) * cluster, leaving SMs idle
+ * where that keeps the wave count, for less L2 pressure and power).  On by default
+ * (FGF8_SM_CAP=0 turns it off at first use); grouped layouts, whose tile count the
+ * host only bounds, always use the full grid.  enable: 1 on, 0 off, anything else
+ * leaves it unchanged.  Returns the previous setting. */
+FGF8_API int fgf8_set_sm_cap(int enable);
+
+/* The cluster count of a static persistent grid for `tiles` cluster tiles of
+ * `cluster` CTAs on `sms` SMs where at most `max_clusters` clusters fit, with the
+ * SM cap on (cap = 1) or off.  Pure host arithmetic (no device needed); it is the
+ * rule every GEMM launch applies. */
+FGF8_API long long fgf8_persistent_clusters(long long tiles, int cluster, int sms, int max_clusters, int cap);
+
 /* Upper bound, in milliseconds, on any single pipeline wait inside a kernel
  * (default 2000; also read from the environment variable FGF8_WAIT_TIMEOUT_MS
  * at first use).  Returns the previous value. */
