@@ -102,8 +102,8 @@ long long align4(long long x) { return (x + 3) / 4 * 4; }
 
 namespace fgf8 {
 
-void set_last_tile(const char* kind, const char* sched, int ctas, int bn) {
-  std::snprintf(g_last_tile, sizeof(g_last_tile), "%s %s %dx%d", kind, sched, ctas, bn);
+void set_last_tile(const char* kind, const char* sched, int ctas, int bn, const char* suffix) {
+  std::snprintf(g_last_tile, sizeof(g_last_tile), "%s %s %dx%d%s", kind, sched, ctas, bn, suffix);
 }
 
 bool pdl_enabled() {

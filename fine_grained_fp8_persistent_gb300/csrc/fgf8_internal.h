@@ -68,7 +68,7 @@ long long persistent_clusters(long long tiles, int cluster, int sms, int max_clu
 // Launches the bounded-wait self-test (selftest.cu).
 int launch_wait_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 // Records the configuration of the GEMM launch this thread makes (fgf8_last_tile).
-void set_last_tile(const char* kind, const char* sched, int ctas, int bn);
+void set_last_tile(const char* kind, const char* sched, int ctas, int bn, const char* suffix = "");
 int device_sm_count();
 int device_max_smem_optin();
 uint32_t* device_status_ptr();

@@ -14,6 +14,11 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
     // at most 64 rows: 64-row A stages, more stages in flight
     if (thin) return launch_persistent<Kind::F8F32, S, 1, 64, 12, 8, 64>(a, tm, tiles, stream);
   }
+  // weight-stationary: 256 rows as two .ws sub-tiles sharing B (dense and masked
+  // layouts; a 256-row tile could straddle two contiguous expert segments)
+  if constexpr (S != Sched::Contiguous) {
+    if (c.ws) return launch_persistent<Kind::F8F32, S, 1, 128, 4, 2, 256>(a, tm, tiles, stream);
+  }
   // pairs: 128-wide tiles so that four partial buffers fit in TMEM
   if (c.ncta == 2) return launch_persistent<Kind::F8F32, S, 2, 128, 8, 4>(a, tm, tiles, stream);
   switch (c.bn) {
@@ -30,7 +35,11 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   // relative tile times (see pick_cfg), measured on M=4096, N=K=7168: the
   // 128-wide tiles and the 256-wide one take the same time per output element,
   // and the 128-wide single-CTA tile is faster on the grouped layouts
+  // (the weight-stationary tile is selectable by FGF8_FORCE_TILE=1x128ws; its
+  // relative time keeps it out of the automatic choice, see the design notes)
   static const TileCfg pair_cands[] = {{2, 128, 17.0}, {1, 256, 34.0}, {1, 128, 16.8}, {1, 64, 16.0}};
+  static const TileCfg ws_cands[] = {{2, 128, 17.0}, {1, 256, 34.0}, {1, 128, 16.8}, {1, 64, 16.0},
+                                     {1, 128, 1e9, true}};
   static const TileCfg single_cands[] = {{1, 256, 34.0}, {1, 128, 16.8}, {1, 64, 16.0}};
   // the contiguous layout takes CTA pairs when its expert segments fit the
   // scheduler's table (pairs are then cut per segment)
@@ -40,15 +49,16 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   const bool fused = a.dq != nullptr;
   if (fused && sched != Sched::Dense) return set_error(2, "fused output quantization: dense layout only");
   const bool pairs = sched != Sched::Contiguous || (a.M + 127) / 128 <= kMaxContiguousPairBlocks;
-  const TileCfg* cands = fused ? fused_cands : pairs ? pair_cands : single_cands;
-  const int n = fused ? kCount(fused_cands) : pairs ? kCount(pair_cands) : kCount(single_cands);
+  const bool ws_ok = sched != Sched::Contiguous;
+  const TileCfg* cands = fused ? fused_cands : ws_ok ? ws_cands : pairs ? pair_cands : single_cands;
+  const int n = fused ? kCount(fused_cands) : ws_ok ? kCount(ws_cands) : pairs ? kCount(pair_cands) : kCount(single_cands);
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
   const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn == 64;
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
-                        thin ? 64 : 128))
+                        thin ? 64 : c.ws ? 256 : 128))
     return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {

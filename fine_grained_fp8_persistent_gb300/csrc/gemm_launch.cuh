@@ -14,6 +14,7 @@ struct TileCfg {
   int ncta;       // 1 = one CTA per tile, 2 = a CTA pair per tile (M = 256)
   int bn;         // tile width
   double t_tile;  // relative time of one cluster tile (measured, see pick_cfg)
+  bool ws = false;  // weight-stationary: one CTA, 256 rows as two .ws sub-tiles
 };
 
 // Entries of a candidate table.
@@ -23,7 +24,7 @@ constexpr int kCount(const TileCfg (&)[N]) { return N; }
 // Tiles of the problem for a configuration, counted per cluster (masked and
 // contiguous pairs: upper bounds).
 inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
-  const long long tm = 128LL * c.ncta;
+  const long long tm = 128LL * c.ncta * (c.ws ? 2 : 1);
   long long mt = (a.M + tm - 1) / tm;
   if (s == Sched::Contiguous && c.ncta == 2) {
     // pairs are cut per expert segment: each segment may end on half a pair
@@ -41,15 +42,18 @@ inline long long tile_count(const GemmArgs& a, Sched s, const TileCfg& c) {
 // narrowest measured ones.  A wide tile wins on large problems; narrow tiles spread
 // skinny problems over more SMs (the DeepGEMM page's unaligned BLOCK_N argument:
 // 112 vs 128 blocks on 132 SMs).
-// FGF8_FORCE_TILE="<ctas per cluster>x<bn>" (e.g. "2x224", "1x128") selects that
-// configuration when it is among the candidates (used by the tests to cover
-// every instantiation).
+// FGF8_FORCE_TILE="<ctas per cluster>x<bn>[ws]" (e.g. "2x224", "1x128", "1x128ws")
+// selects that configuration when it is among the candidates (used by the tests to
+// cover every instantiation).
 inline int pick_cfg(const GemmArgs& a, Sched s, const TileCfg* cands, int n) {
   if (const char* f = std::getenv("FGF8_FORCE_TILE")) {
     int nc = 0, bn = 0;
-    if (std::sscanf(f, "%dx%d", &nc, &bn) == 2)
+    char suffix[4] = {0, 0, 0, 0};
+    const int got = std::sscanf(f, "%dx%d%3s", &nc, &bn, suffix);
+    const bool ws = got == 3 && std::strcmp(suffix, "ws") == 0;
+    if (got >= 2)
       for (int i = 0; i < n; ++i)
-        if (cands[i].ncta == nc && cands[i].bn == bn) return i;
+        if (cands[i].ncta == nc && cands[i].bn == bn && cands[i].ws == ws) return i;
   }
   const long long sms = device_sm_count();
   int best = 0;
@@ -141,7 +145,8 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
                 : KIND == Kind::MXF4 ? "mxf4"
                 : KIND == Kind::NVF4 ? "nvf4"
                                      : "f8f32",
-                SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN);
+                SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN,
+                C::kWS ? "ws" : "");
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, la);
   if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
   return 0;

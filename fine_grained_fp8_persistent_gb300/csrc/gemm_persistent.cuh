@@ -274,14 +274,48 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PairW
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Weight-stationary E4M3 MMA (kind::f8f6f4, cta_group::1, M = 128): mode 1 reads B
+// from shared memory and keeps it in collector buffer 0, mode 2 reads B from that
+// buffer and frees it, mode 0 uses no collector ("GPU GEMM part 4: tcgen05 &
+// Blackwell", section 3.7).
+__device__ __forceinline__ void tc_mma_ws_f8(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc,
+                                             int mode) {
+  if (mode == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.ws.cta_group::1.kind::f8f6f4.collector::b0::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        : "memory");
+  else if (mode == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.ws.cta_group::1.kind::f8f6f4.collector::b0::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.ws.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 template <Kind KIND, Sched SCHED, int NCTA_, int BN_, int STAGES_, int NACC_ = 2, int AROWS_ = 128,
           bool QOUT_ = false>
 struct PCfg {
   static constexpr int NCTA = NCTA_;
   static constexpr int CLUSTER = NCTA;               // a cluster is one CTA or one CTA pair
-  static constexpr int BM = 128;                    // rows per CTA
-  static constexpr int TILE_M = BM * NCTA;
+  static constexpr int BM = 128;                    // rows per CTA (per MMA, per TMEM lane)
+  // Weight-stationary tile (FP32 scales; "GPU GEMM part 4: tcgen05 & Blackwell",
+  // section 3.7): AROWS = 256 rows of A per CTA, computed as two M = 128 sub-tiles
+  // by tcgen05.mma.ws that share each B operand through the MMA unit's collector
+  // buffer (the first fills it, the second uses it last), so one weight tile in
+  // shared memory feeds 256 rows.
+  static constexpr bool kWS = AROWS_ == 2 * BM;
+  static constexpr int MSUB = kWS ? 2 : 1;
+  static constexpr int TILE_M = BM * NCTA * MSUB;
   static constexpr int BN = BN_;
+  static constexpr int PBN = BN * MSUB;             // TMEM columns of one accumulator / K block partial
   static constexpr int BN_LOCAL = BN / NCTA;        // B rows held by each CTA
   static constexpr int STAGES = STAGES_;
   static_assert(NCTA == 1 || NCTA == 2, "one CTA or a pair");
@@ -306,8 +340,10 @@ struct PCfg {
   // flight; the M=128 MMA then reads its upper 64 rows from the shared memory
   // after the stage, which only feeds accumulator rows that are never stored.
   static constexpr int A_ROWS = AROWS_;
-  static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && SCHED == Sched::Dense),
-                "thin A tiles: single CTA, dense layout");
+  static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && SCHED == Sched::Dense) ||
+                    (kWS && KIND == Kind::F8F32 && NCTA == 1 && BN == 128 && SCHED != Sched::Contiguous && !QOUT_),
+                "thin A tiles: single CTA, dense layout; weight-stationary tiles: FP32 scales, one CTA, "
+                "128 columns, dense or masked layout");
   static constexpr int A_BYTES = A_ROWS * 128;
   static constexpr int B_BYTES = BN_LOCAL * 128;
   static constexpr int SFB_ROWS = (BN + 127) / 128 * 128;
@@ -408,7 +444,7 @@ struct PCfg {
   static constexpr int OFF_CLC = (OFF_PREFIX + PREFIX_BYTES + 15) / 16 * 16;
   static constexpr int SMEM_BYTES = OFF_CLC + 16 + 4 * CLC_Q + 1024;
 
-  static constexpr int ACC_COLS = NACC * BN;
+  static constexpr int ACC_COLS = NACC * PBN;
   static constexpr int SF_COL0 = ACC_COLS;
   static constexpr int TMEM_USED = ACC_COLS + (kBS ? SF_SLOTS * SF_SLOT_COLS : 0);
   static constexpr int TMEM_ALLOC = TMEM_USED <= 32    ? 32
@@ -933,7 +969,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
       const uint32_t idesc0 = C::kMX    ? idesc_mxf8(BN, C::TILE_M, 0, 0)
                               : C::kFP4 ? idesc_fp4(BN, C::TILE_M, KIND == Kind::MXF4)
-                                        : idesc_dense(in_fmt, in_fmt, BN, C::TILE_M);
+                                        : idesc_dense(in_fmt, in_fmt, BN, C::kWS ? C::BM : C::TILE_M);
       // descriptors are linear in the address (start field = address >> 4)
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
@@ -941,6 +977,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         Tile tl;
         if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
         uint32_t sf_col = 0;
+        const bool ws_two = C::kWS && tl.row_limit > C::BM;   // weight-stationary: both sub-tiles hold rows
+        (void)ws_two;
         for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
           named_bar_sync(C::HANDOFF_BAR, 64);
           ptx::tc_fence_after();
@@ -958,7 +996,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
                 // FP32 scales: K block j of the unit has its own partial buffer
                 // in the unit's slot
                 const int buf = C::kF32S ? acc * C::KPU + j : acc;
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * C::PBN);
                 const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
                 const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
                 const uint64_t bd = bdesc0 + stage * (C::B_BYTES >> 4);
@@ -978,8 +1016,22 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
                     sfb = sf_col + 4u * C::WG + static_cast<uint32_t>(C::NB_COLS * wi);
                     idk = idesc0 | (fid << 4) | (fid << 29);
                   }
-                  tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), idk,
-                                     sfa, sfb, accum);
+                  if constexpr (C::kWS) {
+                    // sub-tile 1 (A rows 128-255, 16 KB into the stage) reuses sub-tile
+                    // 0's B from the collector; a tile with at most 128 valid rows
+                    // skips it
+                    const uint64_t ka = ad + (k * C::MMA_K_BYTES >> 4);
+                    const uint64_t kbd = bd + (k * C::MMA_K_BYTES >> 4);
+                    if (ws_two) {
+                      tc_mma_ws_f8(d_tmem, ka, kbd, idk, accum, 1);
+                      tc_mma_ws_f8(d_tmem + BN, ka + ((C::BM * 128) >> 4), kbd, idk, accum, 2);
+                    } else {
+                      tc_mma_ws_f8(d_tmem, ka, kbd, idk, accum, 0);
+                    }
+                  } else {
+                    tc_mma<NCTA, KIND>(d_tmem, ad + (k * C::MMA_K_BYTES >> 4), bd + (k * C::MMA_K_BYTES >> 4), idk,
+                                       sfa, sfb, accum);
+                  }
                 }
               }
             }
@@ -1364,10 +1416,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     aborted = !ok;
   } else {
     // ============================================================ promotion
+    // Warp (q, h): TMEM lane quarter q; h selects the column half of the partial,
+    // or, on the weight-stationary tile, the 128-row sub-tile (all its columns).
     ctl.role_bit = FGF8_DEVERR_ROLE_EPILOGUE;
-    constexpr int HALF = BN / 2;
+    constexpr int HALF = C::kWS ? BN : BN / 2;        // columns per warp
     const uint32_t q = warp & 3u;
     const int h = static_cast<int>(warp - C::EPI_WARP0) >> 2;
+    const int row_off_h = C::kWS ? h * C::BM : 0;      // first row of this warp's sub-tile
+    const int col_off_h = C::kWS ? 0 : h * HALF;       // first column of this warp's half
     const bool bf16 = args.out_bf16 != 0;
     const int nkb128 = K / 128;
     const int nnb = (N + 127) / 128;
@@ -1389,10 +1445,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       Tile st;
       seq_valid(s_sq, st);
       if (s_sq.t == kSeqEnd) return;
-      const int c0 = st.n_blk * BN + h * HALF;
-      if (r < st.row_limit)
+      const int c0 = st.n_blk * BN + col_off_h;
+      if (row_off_h + r < st.row_limit)
         s_pa = args.sfa_f32 + (SCHED == Sched::Masked ? static_cast<size_t>(st.group) * nkb128 * ld_a : 0) +
-               (st.m_blk + r);
+               (st.m_blk + row_off_h + r);
       if (c0 < N) s_pb = args.sfb_f32 + (static_cast<size_t>(st.group) * nnb + c0 / 128) * nkb128;
     };
     float na[C::KPU], nb[C::KPU];  // the next unit's scales, in flight
@@ -1435,7 +1491,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         uint32_t(&nxt)[CH] = (c & 1) ? va : vb;
         if (c + 1 < TOT) {
           const int n1 = c + 1;
-          tmem_ld_chunk(taddr + static_cast<uint32_t>((n1 / NCH) * BN + CH * (n1 % NCH)), nxt);
+          tmem_ld_chunk(taddr + static_cast<uint32_t>((n1 / NCH) * C::PBN + CH * (n1 % NCH)), nxt);
         } else {
           ptx::tc_fence_before();
           __syncwarp();
@@ -1455,7 +1511,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     for (Seq sq = seq_begin(); ok && sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
       if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
-      bool row_ok = r < tl.row_limit;
+      bool row_ok = row_off_h + r < tl.row_limit;
+      // weight-stationary: a sub-tile without valid rows got no MMAs; its warps only
+      // keep the slot handshake
+      const bool idle = C::kWS && row_off_h >= tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {
           const int g = __ldg(args.m_indices + tl.a_row0 + r);
@@ -1465,7 +1524,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
           }
         }
       }
-      const int col0 = tl.n_blk * BN + h * HALF;
+      const int col0 = tl.n_blk * BN + col_off_h;
 #pragma unroll
       for (int i = 0; i < HALF; ++i) accv[i] = 0.0f;
       for (int kb0 = 0; kb0 < nkb; kb0 += C::KPU) {
@@ -1476,10 +1535,14 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         if (!pwait(bar(C::BAR_ACC_FULL + pslot), pphase, ctl)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t taddr =
-            tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pslot * C::KPU * BN + h * HALF);
+            tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(pslot * C::KPU * C::PBN + h * HALF);
         // a tile's last unit may hold fewer K blocks
         const int nk = min(C::KPU, nkb - kb0);
-        if (nk == C::KPU) promote_unit(std::integral_constant<int, C::KPU>{}, sc, taddr);
+        if (idle) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + pslot));
+        } else if (nk == C::KPU) promote_unit(std::integral_constant<int, C::KPU>{}, sc, taddr);
         else if (C::KPU > 3 && nk == 3) promote_unit(std::integral_constant<int, (C::KPU > 3 ? 3 : 1)>{}, sc, taddr);
         else if (C::KPU > 2 && nk == 2) promote_unit(std::integral_constant<int, (C::KPU > 2 ? 2 : 1)>{}, sc, taddr);
         else promote_unit(std::integral_constant<int, 1>{}, sc, taddr);
@@ -1498,7 +1561,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         }
       }
       if (row_ok) {
-        const size_t row_off = static_cast<size_t>(tl.a_row0 + r) * static_cast<size_t>(N);
+        const size_t row_off = static_cast<size_t>(tl.a_row0 + row_off_h + r) * static_cast<size_t>(N);
 #pragma unroll
         for (int c = 0; c < HALF / 32; ++c) store_row32(args.D, row_off, col0 + 32 * c, N, accv + 32 * c, bf16);
       }

@@ -164,7 +164,7 @@ def test_host_memory_is_rejected(fg, dev):
 # as "<CTAs per cluster>x<BN>": one CTA per tile, or a CTA pair (M = 256, B split
 # across the pair).
 MXF8_TILES = ["2x256", "2x224", "2x128", "1x224", "1x128", "1x64", "1x48", "1x32"]
-F8F32_TILES = ["2x128", "1x256", "1x128", "1x64"]
+F8F32_TILES = ["2x128", "1x256", "1x128", "1x64", "1x128ws"]
 F16_TILES = ["2x256", "2x224", "1x128"]
 
 

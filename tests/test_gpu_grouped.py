@@ -206,7 +206,7 @@ def test_masked_ue8m0_every_tile(fg, dev, oracle, monkeypatch, tile):
     assert np.isnan(o[~v]).all()
 
 
-@pytest.mark.parametrize("tile", ["2x128", "1x256", "1x128"])
+@pytest.mark.parametrize("tile", ["2x128", "1x256", "1x128", "1x128ws"])
 def test_masked_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     masked = (0, 256, 17, 200)
@@ -284,3 +284,20 @@ def test_masked_in_a_cuda_graph(fg, dev, oracle):
         v = valid.astype(bool)
         gemm_close(o[v], ref[v], f"graph replay {masked}")
         assert np.isnan(o[~v]).all()
+
+
+def test_masked_weight_stationary_full_size(fg, dev, oracle, monkeypatch):
+    """The masked decode configuration (32 experts, Mmax = 256, N = 7168, K = 2048,
+    FP32 scales) on the weight-stationary tile: every valid element against the
+    oracle's dequantize-then-matmul form; rows past masked_m stay unwritten."""
+    monkeypatch.setenv("FGF8_FORCE_TILE", "1x128ws")
+    G, Mmax, N, K = 32, 256, 7168, 2048
+    masked = inputs.masked_rows(G, Mmax, 10).numpy()
+    case = _masked_case(G, Mmax, N, K, 0, 11)
+    out = _run_masked(fg, dev, case, tuple(int(m) for m in masked), 0)
+    assert fg.last_tile() == "f8f32 masked 1x128ws"
+    ref, valid = oracle.grouped_masked_dequant(*case, masked.astype(np.int32), 0)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    gemm_close(o[v], ref[v], "masked ws full size")
+    assert np.isnan(o[~v]).all()

@@ -72,7 +72,7 @@ def _fp8_operands(fg, dev, M, N, K, fmt, seed):
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("tile", [None, "1x128", "2x128"])
+@pytest.mark.parametrize("tile", [None, "1x128", "2x128", "1x128ws"])
 def test_dense_fp8_same_bits(fg, dev, restore, monkeypatch, fmt, tile):
     if tile:
         monkeypatch.setenv("FGF8_FORCE_TILE", tile)
