@@ -82,9 +82,6 @@ template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC = 2, in
 int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, cudaStream_t stream) {
   using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   static_assert(C::SMEM_BYTES <= kMaxSmemOptin, "shared memory budget");
-  // a thin A stage is followed by at least 8 KB of the CTA's shared memory (the
-  // MMA's unused upper rows read there)
-  static_assert(C::A_ROWS == C::BM || C::STAGES * C::B_BYTES >= 64 * 128, "thin A overread");
   auto* fn = &gemm_persistent<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   if ((a.dq != nullptr) != QOUT) return set_error(2, "output quantization and kernel disagree");
   constexpr int CL = C::CLUSTER;

@@ -16,11 +16,11 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
     }
     // one 256-wide accumulator (drained by 8 epilogue warps)
     if (c.ncta == 2 && c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1>(a, tm, tiles, stream);
-    if (thin) {  // at most 64 rows: 64-row A stages, twice the stages in flight
+    if (thin) {  // at most 64 rows: 64-row A boxes, A and B interleaved per 16 KB stage
       switch (c.bn) {
         case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 64>(a, tm, tiles, stream);
         case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 12, 2, 64>(a, tm, tiles, stream);
-        default: return launch_persistent<Kind::MXF8, S, 1, 32, 16, 2, 64>(a, tm, tiles, stream);
+        default: return launch_persistent<Kind::MXF8, S, 1, 32, 12, 2, 64>(a, tm, tiles, stream);
       }
     }
   }

@@ -335,11 +335,23 @@ struct PCfg {
   static constexpr int KB_ELEMS = (KIND == Kind::F16) ? 64 : kFP4 ? 256 : 128;
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
-  // Rows of A staged per K block.  A thin tile (64 rows, for a dense GEMM with at
-  // most 64 rows) halves the A stage so that twice as many stages of B are in
-  // flight; the M=128 MMA then reads its upper 64 rows from the shared memory
-  // after the stage, which only feeds accumulator rows that are never stored.
-  static constexpr int A_ROWS = AROWS_;
+  // Rows of A per K block.  A thin tile (AROWS = 64, for a dense GEMM with at most
+  // 64 rows) loads 64-row A boxes.  With FP32 scales it also stages 64 rows and
+  // issues M = 64 MMAs ("Blackwell Tensor Core: tcgen05.mma": the cta_group::1
+  // M = 64 accumulator, Layout F, puts row m in TMEM lane 32 (m / 16) + m % 16, so
+  // each lane quarter holds 16 rows in its first 16 lanes), which leaves room for
+  // more stages.  The block-scaled MMA of one CTA has M = 128 only: there each
+  // stage holds its 64 A rows, then its own B rows, padded to 16 KB, so the MMA's
+  // upper 64 rows read this stage's landed B and padding (never a stage that TMA
+  // is filling) and only feed accumulator rows that are never stored.
+  static constexpr bool kThin = AROWS_ < BM;
+  static constexpr bool kThinM64 = kThin && !(KIND == Kind::MXF8 || KIND == Kind::MXF4 || KIND == Kind::NVF4);
+  static constexpr bool kInterleave = kThin && !kThinM64;
+  static constexpr int A_LOAD_ROWS = AROWS_;                           // rows of one A box
+  static constexpr int A_ROWS = AROWS_;                                // rows of one A stage
+  static constexpr int MMA_M = kThinM64 ? 64 : (kWS ? BM : BM * NCTA);   // rows per MMA instruction
+  static constexpr int QROWS = kThinM64 ? 16 : 32;                       // accumulator rows per lane quarter
+  static_assert(!kThin || (NCTA == 1 && SCHED == Sched::Dense), "thin A tiles: single CTA, dense layout");
   static_assert(A_ROWS == BM || (A_ROWS == 64 && NCTA == 1 && SCHED == Sched::Dense) ||
                     (kWS && KIND == Kind::F8F32 && NCTA == 1 && BN == 128 && SCHED != Sched::Contiguous && !QOUT_),
                 "thin A tiles: single CTA, dense layout; weight-stationary tiles: FP32 scales, one CTA, "
@@ -397,9 +409,13 @@ struct PCfg {
   static constexpr int SF_RING = 4;                                // scale-word groups in SMEM
   static constexpr int SFA_RING_BYTES = kBS ? WG * BM * 4 : 0;
   static constexpr int SFB_RING_BYTES = kBS ? WG * SFB_ROWS * 4 : 0;
+  static constexpr int STAGE_BYTES = 16384;        // interleaved stage: A, then B, then padding
+  static_assert(!kInterleave || A_BYTES + B_BYTES <= STAGE_BYTES, "interleaved stage");
+  static constexpr int A_STRIDE = kInterleave ? STAGE_BYTES : A_BYTES;
+  static constexpr int B_STRIDE = kInterleave ? STAGE_BYTES : B_BYTES;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_B = kInterleave ? A_BYTES : OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = kInterleave ? STAGES * STAGE_BYTES : OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + SF_RING * SFA_RING_BYTES;
   static constexpr int OFF_BAR = (OFF_SFB + SF_RING * SFB_RING_BYTES + 7) / 8 * 8;
   static constexpr int BAR_FULL = 0;                              // UNITS
@@ -453,7 +469,7 @@ struct PCfg {
                                     : TMEM_USED <= 256 ? 256
                                                        : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
-  static constexpr uint32_t A_TX = NCTA * (A_BYTES + B_BYTES);   // bytes landing on `full`
+  static constexpr uint32_t A_TX = NCTA * (A_LOAD_ROWS * 128 + B_BYTES);   // bytes landing on `full`
   static_assert(kF32S ? NACC >= 2 : (NACC == 2 || (NACC == 1 && BN == 256 && kBS)),
                 "accumulator buffers");
   static constexpr uint32_t SF_TX = WG * (BM * 4 + BN * 4);         // bytes landing on `sf_loaded`
@@ -947,8 +963,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
           for (int j = 0; j < nk; ++j) {
             const int stage = unit * C::KPU + j;
             const int kb = kb0 + j;
-            tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_BYTES, &tm_a, full, kb * C::BK, tl.a_row0);
-            tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_BYTES, &tm_b, full, kb * C::BK, tl.b_row0);
+            tma_load_ab<NCTA>(sbase + C::OFF_A + stage * C::A_STRIDE, &tm_a, full, kb * C::BK, tl.a_row0);
+            tma_load_ab<NCTA>(sbase + C::OFF_B + stage * C::B_STRIDE, &tm_b, full, kb * C::BK, tl.b_row0);
           }
         }
         __syncwarp();
@@ -967,9 +983,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       int acc = 0;
       uint32_t gctr = 0u;            // scale-word groups consumed so far (all tiles)
       const uint32_t in_fmt = (KIND == Kind::F16 && args.in_bf16) ? 1u : 0u;
-      const uint32_t idesc0 = C::kMX    ? idesc_mxf8(BN, C::TILE_M, 0, 0)
-                              : C::kFP4 ? idesc_fp4(BN, C::TILE_M, KIND == Kind::MXF4)
-                                        : idesc_dense(in_fmt, in_fmt, BN, C::kWS ? C::BM : C::TILE_M);
+      const uint32_t idesc0 = C::kMX    ? idesc_mxf8(BN, C::MMA_M, 0, 0)
+                              : C::kFP4 ? idesc_fp4(BN, C::MMA_M, KIND == Kind::MXF4)
+                                        : idesc_dense(in_fmt, in_fmt, BN, C::MMA_M);
       // descriptors are linear in the address (start field = address >> 4)
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
@@ -998,8 +1014,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
                 const int buf = C::kF32S ? acc * C::KPU + j : acc;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * C::PBN);
                 const uint32_t stage = static_cast<uint32_t>(unit * C::KPU + j);
-                const uint64_t ad = adesc0 + stage * (C::A_BYTES >> 4);
-                const uint64_t bd = bdesc0 + stage * (C::B_BYTES >> 4);
+                const uint64_t ad = adesc0 + stage * (C::A_STRIDE >> 4);
+                const uint64_t bd = bdesc0 + stage * (C::B_STRIDE >> 4);
                 // UE8M0 FP8: byte kb % 4 of the group's scale word (a_sf_id, b_sf_id)
                 const uint32_t sfid = static_cast<uint32_t>(kb & 3);
                 const uint32_t id = C::kMX ? (idesc0 | (sfid << 4) | (sfid << 29)) : idesc0;
@@ -1267,8 +1283,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
-      const int r = static_cast<int>(q * 32 + lane);
-      bool row_ok = r < tl.row_limit;
+      const int r = static_cast<int>(q * C::QROWS + lane);
+      bool row_ok = lane < static_cast<uint32_t>(C::QROWS) && r < tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {
           const int g = __ldg(args.m_indices + tl.a_row0 + r);
@@ -1367,8 +1383,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
       if (!pwait(bar(C::BAR_ACC_FULL + acc), acc_phase, ctl)) { ok = false; break; }
       ptx::tc_fence_after();
-      const int r = static_cast<int>(q * 32 + lane);
-      bool row_ok = r < tl.row_limit;
+      const int r = static_cast<int>(q * C::QROWS + lane);
+      bool row_ok = lane < static_cast<uint32_t>(C::QROWS) && r < tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {
           const int g = __ldg(args.m_indices + tl.a_row0 + r);
@@ -1428,7 +1444,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     const int nkb128 = K / 128;
     const int nnb = (N + 127) / 128;
     const int ld_a = (M + 3) / 4 * 4;
-    const int r = static_cast<int>(q * 32 + lane);
+    const int r = static_cast<int>(q * C::QROWS + lane);
     // The scale stream walks the same tiles and units as the promotion below, one
     // unit earlier, with plain global loads into registers (the MMAs keep shared
     // memory busy, so scales do not go through it).  The loads are unconditional
@@ -1446,7 +1462,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       seq_valid(s_sq, st);
       if (s_sq.t == kSeqEnd) return;
       const int c0 = st.n_blk * BN + col_off_h;
-      if (row_off_h + r < st.row_limit)
+      if (lane < static_cast<uint32_t>(C::QROWS) && row_off_h + r < st.row_limit)
         s_pa = args.sfa_f32 + (SCHED == Sched::Masked ? static_cast<size_t>(st.group) * nkb128 * ld_a : 0) +
                (st.m_blk + row_off_h + r);
       if (c0 < N) s_pb = args.sfb_f32 + (static_cast<size_t>(st.group) * nnb + c0 / 128) * nkb128;
@@ -1511,10 +1527,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     for (Seq sq = seq_begin(); ok && sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
       if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
-      bool row_ok = row_off_h + r < tl.row_limit;
-      // weight-stationary: a sub-tile without valid rows got no MMAs; its warps only
-      // keep the slot handshake
-      const bool idle = C::kWS && row_off_h >= tl.row_limit;
+      bool row_ok = lane < static_cast<uint32_t>(C::QROWS) && row_off_h + r < tl.row_limit;
+      // a warp whose rows are all past the tile's valid rows (the last M tile of
+      // a masked expert or contiguous segment, or a weight-stationary sub-tile that
+      // got no MMAs) promotes nothing and only keeps the slot handshake
+      const bool idle = row_off_h + static_cast<int>(q) * C::QROWS >= tl.row_limit;
       if constexpr (SCHED == Sched::Contiguous) {
         if (row_ok) {
           const int g = __ldg(args.m_indices + tl.a_row0 + r);
