@@ -43,6 +43,10 @@ struct GemmArgs {
   uint8_t* dq;
   void* sfd;
   int dq_ue8m0;               // 1: UE8M0 scales, 0: FP32 scales
+  // Thin tiles (at most 64 rows): rows of the A box, a multiple of 8 that covers M
+  // (the A tensor has only M rows; the stage rows past the box are never stored).
+  // 0 = the tile's full 64.
+  int a_box_rows;
   // Tile scheduling: 0 = static round robin over a persistent grid; 1 = cluster
   // launch control (a grid of one cluster per tile; running clusters cancel the
   // clusters not yet launched and take their tiles)

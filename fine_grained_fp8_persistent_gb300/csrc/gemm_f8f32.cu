@@ -55,16 +55,18 @@ int launch_gemm_f8f32(const GemmArgs& a, Sched sched, const void* Aq, const void
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
+  GemmArgs at = a;
   const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn == 64;
+  at.a_box_rows = thin ? thin_a_box_rows(a.M) : 0;
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
-                        thin ? 64 : c.ws ? 256 : 128))
+                        thin ? thin_a_box_rows(a.M) : c.ws ? 256 : 128))
     return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, thin, stream);
-    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, false, stream);
-    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, false, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, at, tm, tiles, thin, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, at, tm, tiles, false, stream);
+    default: return launch_cfg<Sched::Masked>(c, at, tm, tiles, false, stream);
   }
 }
 

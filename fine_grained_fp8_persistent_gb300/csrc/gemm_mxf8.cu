@@ -16,7 +16,7 @@ int launch_cfg(const TileCfg& c, const GemmArgs& a, const TensorMaps& tm, long l
     }
     // one 256-wide accumulator (drained by 8 epilogue warps)
     if (c.ncta == 2 && c.bn == 256) return launch_persistent<Kind::MXF8, S, 2, 256, 6, 1>(a, tm, tiles, stream);
-    if (thin) {  // at most 64 rows: 64-row A boxes, A and B interleaved per 16 KB stage
+    if (thin) {  // at most 64 rows: 64-row A stages (boxes of M rounded to 8), A and B interleaved per 16 KB stage
       switch (c.bn) {
         case 64: return launch_persistent<Kind::MXF8, S, 1, 64, 12, 2, 64>(a, tm, tiles, stream);
         case 48: return launch_persistent<Kind::MXF8, S, 1, 48, 12, 2, 64>(a, tm, tiles, stream);
@@ -64,10 +64,12 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
   const TileCfg c = cands[pick_cfg(a, sched, cands, n)];
   const long long a_rows = (sched == Sched::Masked) ? static_cast<long long>(a.G) * a.M : a.M;
   const long long b_rows = static_cast<long long>(a.G) * a.N;
+  GemmArgs at = a;
   const bool thin = sched == Sched::Dense && a.M <= 64 && c.ncta == 1 && c.bn <= 64;
+  at.a_box_rows = thin ? thin_a_box_rows(a.M) : 0;
   TensorMaps tm;
   if (make_operand_maps(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Aq, a_rows, Bq, b_rows, a.K, c.bn / c.ncta,
-                        thin ? 64 : 128))
+                        thin ? thin_a_box_rows(a.M) : 128))
     return 4;
   // Packed UE8M0 scale words: one int32 per row per four K blocks, rows padded to 4.
   const long long kq = (a.K / 128 + 3) / 4;
@@ -80,9 +82,9 @@ int launch_gemm_mxf8(const GemmArgs& a, Sched sched, const void* Aq, const void*
     return 4;
   const long long tiles = tile_count(a, sched, c);
   switch (sched) {
-    case Sched::Dense: return launch_cfg<Sched::Dense>(c, a, tm, tiles, thin, stream);
-    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, a, tm, tiles, false, stream);
-    default: return launch_cfg<Sched::Masked>(c, a, tm, tiles, false, stream);
+    case Sched::Dense: return launch_cfg<Sched::Dense>(c, at, tm, tiles, thin, stream);
+    case Sched::Contiguous: return launch_cfg<Sched::Contiguous>(c, at, tm, tiles, false, stream);
+    default: return launch_cfg<Sched::Masked>(c, at, tm, tiles, false, stream);
   }
 }
 

@@ -951,6 +951,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     int unit = 0;
     uint32_t phase = 0;
     bool ok = true;
+    // bytes landing per K block: a thin tile's A box may be shorter than its stage
+    const uint32_t a_tx = (C::kThin && args.a_box_rows > 0)
+                              ? static_cast<uint32_t>(NCTA * (args.a_box_rows * 128 + C::B_BYTES))
+                              : C::A_TX;
     for (Seq sq = seq_begin(); ok && sq.t != kSeqEnd; seq_next(sq)) {
       Tile tl;
       if (sq.t >= num_tiles || !get_tile(sq.t, tl)) continue;
@@ -959,7 +963,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
         if (lane == 0) {
           const int nk = min(C::KPU, nkb - kb0);     // K blocks in this unit (the tail may be short)
           const uint32_t full = lbar(C::BAR_FULL + unit);
-          if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + unit), static_cast<uint32_t>(nk) * C::A_TX);
+          if (leader) ptx::mbar_arrive_expect_tx(bar(C::BAR_FULL + unit), static_cast<uint32_t>(nk) * a_tx);
           for (int j = 0; j < nk; ++j) {
             const int stage = unit * C::KPU + j;
             const int kb = kb0 + j;

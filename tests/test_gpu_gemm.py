@@ -188,13 +188,15 @@ def test_fp8_f32scale_every_tile(fg, dev, oracle, monkeypatch, tile, M, N, K):
     gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, 0), f"f32 {tile} {M}x{N}x{K}")
 
 
-# At most 64 rows the decode tiles stage 64-row A boxes (more stages in flight):
-# ragged N, K with an odd number of 128-blocks, and more K blocks than stages.
+# At most 64 rows the decode tiles stage 64-row A tiles (more stages in flight),
+# loaded by boxes of M rounded up to 8 rows: ragged N, K with an odd number of
+# 128-blocks, more K blocks than stages, and boxes of 8, 16, 40 and 64 rows.
 THIN_TILES = [(1, "1x64"), (1, "1x48"), (1, "1x32"), (0, "1x64")]
 
 
 @pytest.mark.parametrize("fmt,tile", THIN_TILES)
-@pytest.mark.parametrize("M,N,K", [(64, 448, 1920), (37, 200, 2048), (1, 96, 3968)])
+@pytest.mark.parametrize("M,N,K", [(64, 448, 1920), (37, 200, 2048), (1, 96, 3968), (9, 136, 1024),
+                                   (16, 264, 512)])
 def test_fp8_thin_a_tiles(fg, dev, oracle, monkeypatch, fmt, tile, M, N, K):
     monkeypatch.setenv("FGF8_FORCE_TILE", tile)
     case = _fp8_case(M, N, K, fmt, 500 + M + K)
