@@ -7,7 +7,8 @@
 // E2M1 + E4M3 per 16; section 7.1: two 4-bit elements per byte along K.
 //   MXFP4 scale 2^e, e = ceil(log2(amax / 6)) (FP32 quotient), codes E2M1(x 2^-e);
 //   NVFP4 scale s = E4M3(amax / 6) (FP32 quotient, nearest even, saturating),
-//         codes E2M1(x / s) with an FP32 division (0 when s is 0);
+//         codes E2M1(x / s) of the FP32 quotient (0 when s is 0; computed by
+//         nv_quotient without a full division);
 //   an all-zero group has scale 1; E2M1 rounds to nearest even, saturating at 6.
 //
 // An HBM stream: 2 bytes read and half a byte written per element, plus one
@@ -41,6 +42,36 @@ __device__ __forceinline__ int mx_exponent(float amax) {
     e = msb - 149 + ((man & (man - 1u)) != 0u ? 1 : 0);
   }
   return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// E2M1(x / s) for NVFP4 without a full IEEE division, giving the code the
+// correctly rounded FP32 quotient gives.  x is a bf16 value (at most 8
+// significant bits) and s an E4M3 scale (at most 4), so x / s is either exactly
+// one of the E2M1 rounding midpoints m (0.25, 0.75, ..., 5: at most 3 significant
+// bits, and m * s is exact in FP32) or at least 2^-8 (relative) away from every
+// one of them: x - m * s is a nonzero multiple of the coarser of the two values'
+// last-bit weights.  q0 = x * (1 / s) is within 2^-23 of x / s, so it lies on the
+// same side of every midpoint except in the exact case; one correction step with
+// the exact remainder, q1 = q0 + (x - q0 * s) / s (both by FMA), lands exactly on
+// m then (its error is ~2^-46 relative).  cvt then rounds q1 to nearest even as it
+// would the correctly rounded quotient.  s comes from the group's own max |x|, so
+// |x / s| stays below ~12 and nothing overflows.  The correction turns x = -0
+// into +0, so the sign is taken from x (as the quotient's is).  Two values per
+// call, on paired FP32 instructions; r = 1 / s, ns = -s.
+__device__ __forceinline__ void nv_quotient2(float x0, float x1, float r, float ns, float& y0, float& y1) {
+  float q0, q1;
+  asm("{\n\t.reg .b64 x, rr, nn, q, e;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 rr, {%4, %4};\n\t"
+      "mov.b64 nn, {%5, %5};\n\t"
+      "mul.rn.f32x2 q, x, rr;\n\t"
+      "fma.rn.f32x2 e, q, nn, x;\n\t"
+      "fma.rn.f32x2 q, e, rr, q;\n\t"
+      "mov.b64 {%0, %1}, q;\n\t}"
+      : "=f"(q0), "=f"(q1)
+      : "f"(x0), "f"(x1), "f"(r), "f"(ns));
+  y0 = copysignf(q0, x0);
+  y1 = copysignf(q1, x1);
 }
 
 // 2^-e as an FP32 value, e in [-127, 127].
@@ -81,10 +112,11 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(const __nv_bfloat16* 
   }
   if (!NV) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // 32-element group: two lanes
   uint32_t byte;
-  float mul = 1.0f, s = 1.0f;
+  float mul = 1.0f, s = 1.0f, rs = 1.0f;
   if (NV) {
     byte = amax == 0.0f ? 0x38u : static_cast<uint32_t>(ptx::cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu);
     s = ptx::e4m3_value(byte);
+    rs = s == 0.0f ? 0.0f : __frcp_rn(s);
   } else {
     const int e = mx_exponent(amax);
     byte = static_cast<uint32_t>(e + 127);
@@ -92,10 +124,22 @@ __global__ void __launch_bounds__(256) quantize_fp4_kernel(const __nv_bfloat16* 
   }
   if (active) {
     float q0[8], q1[8];
+    if (NV) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      q0[i] = NV ? (s == 0.0f ? 0.0f : __fdiv_rn(f[i], s)) : f[i] * mul;
-      q1[i] = NV ? (s == 0.0f ? 0.0f : __fdiv_rn(f[8 + i], s)) : f[8 + i] * mul;
+      for (int i = 0; i < 8; i += 2) {
+        nv_quotient2(f[i], f[i + 1], rs, -s, q0[i], q0[i + 1]);
+        nv_quotient2(f[8 + i], f[9 + i], rs, -s, q1[i], q1[i + 1]);
+      }
+      if (s == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q0[i] = q1[i] = 0.0f;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        q0[i] = f[i] * mul;
+        q1[i] = f[8 + i] * mul;
+      }
     }
     *reinterpret_cast<uint2*>(Xq + static_cast<size_t>(r) * (K / 2) + col0 / 2) =
         make_uint2(ptx::cvt_e2m1x8(q0), ptx::cvt_e2m1x8(q1));

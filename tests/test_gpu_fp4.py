@@ -58,6 +58,46 @@ def test_quantize_fp4_bit_exact(fg, dev, oracle, fmt, R, K):
     assert np.array_equal(sf.cpu().numpy(), osf), "scale words differ"
 
 
+def _every_value_under_every_scale():
+    """NVFP4 groups covering every (bf16 value, E4M3 scale) pair a group can hold:
+    for each positive finite E4M3 scale s, groups led by amax = 6 s (whose scale
+    is exactly s) followed by every bf16 value of magnitude <= amax, both signs
+    (zeros, subnormals and values exactly on the E2M1 rounding midpoints
+    included).  Rows of 4096 elements, padded with zeros."""
+    import oracle
+    bits = np.arange(0x8000, dtype=np.uint32)
+    pos = (bits << 16).view(np.float32)
+    pos = pos[np.isfinite(pos)]
+    scales = oracle.e4m3_decode(np.arange(1, 127, dtype=np.uint8))
+    groups = []
+    for sv in scales:
+        amax = np.float32(6.0 * sv)
+        assert float(amax) == 6.0 * float(sv)          # exact in bf16 and FP32
+        vals = pos[pos <= amax]
+        vals = np.concatenate([vals, -vals])
+        vals = np.concatenate([vals, np.zeros((-len(vals)) % 15, np.float32)])
+        body = vals.reshape(-1, 15)
+        groups.append(np.concatenate([np.full((len(body), 1), amax, np.float32), body], axis=1))
+    g = np.concatenate(groups).reshape(-1)
+    g = np.concatenate([g, np.zeros((-len(g)) % 4096, np.float32)])
+    x = torch.from_numpy(g.reshape(-1, 4096)).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(g.reshape(-1, 4096)))   # every value is a bf16 value
+    return x
+
+
+def test_quantize_nvfp4_every_value_and_scale(fg, dev, oracle):
+    """NVFP4 codes of every bf16 value under every E4M3 scale, bit-exact against
+    the oracle's FP32 division (the kernel decides them without one)."""
+    x = _every_value_under_every_scale()
+    xq, sf = fg.quantize_fp4(x.to(dev), 1)
+    oq, osf = oracle.quantize_fp4(x.float().numpy(), 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(sf.cpu().numpy(), osf), "scale words differ"
+    got = xq.cpu().numpy()
+    bad = np.nonzero(got != oq)
+    assert bad[0].size == 0, f"{bad[0].size} code bytes differ, first at {bad[0][0]}, {bad[1][0]}"
+
+
 @functools.lru_cache(maxsize=6)
 def _fp4_case(M, N, K, fmt, seed):
     import oracle
