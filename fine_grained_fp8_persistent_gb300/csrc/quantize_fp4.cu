@@ -52,8 +52,8 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 // one of them: x - m * s is a nonzero multiple of the coarser of the two values'
 // last-bit weights.  q0 = x * (1 / s) is within 2^-23 of x / s, so it lies on the
 // same side of every midpoint except in the exact case; one correction step with
-// the exact remainder, q1 = q0 + (x - q0 * s) / s (both by FMA), lands exactly on
-// m then (its error is ~2^-46 relative).  cvt then rounds q1 to nearest even as it
+// the exact remainder (the FMA remainder step of Markstein's division), q1 = q0 +
+// (x - q0 * s) * (1 / s), lands exactly on m then (its error is ~2^-46 relative).  cvt then rounds q1 to nearest even as it
 // would the correctly rounded quotient.  s comes from the group's own max |x|, so
 // |x / s| stays below ~12 and nothing overflows.  The correction turns x = -0
 // into +0, so the sign is taken from x (as the quotient's is).  Two values per
