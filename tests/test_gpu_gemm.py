@@ -70,6 +70,17 @@ def test_fp8_dense_full_size(fg, dev, oracle, fmt, M):
     gemm_close(got[r, c], oracle.gemm_fp8_entries(*case, fmt, r, c), f"fp8 full M={M} fmt{fmt} (triple loop)")
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N", [(130, 264), (64, 200)])
+def test_fp8_long_k(fg, dev, oracle, fmt, M, N):
+    """K = 32768: 256 K blocks, 64 scale words per row, hundreds of pipeline
+    units and scale groups per tile (every ring wraps many times)."""
+    K = 32768
+    case = _fp8_case(M, N, K, fmt, 900 + M)
+    out = _run_fp8(fg, dev, case, fmt, M, N)
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_fp8(*case, fmt), f"long K {M}x{N}x{K} fmt{fmt}")
+
+
 def test_ue8m0_full_size_repeated_pair_tiles(fg, dev, oracle, monkeypatch):
     """UE8M0 scales at 4096 x 7168 x 7168 on the CTA-pair tiles, several launches
     each, every element against the oracle (the scale words pass through the same

@@ -144,6 +144,39 @@ def _run_masked(fg, dev, case, masked, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts", [(300,), (128,), (1,)])
+def test_contiguous_single_expert(fg, dev, oracle, fmt, counts):
+    """One expert (G = 1): a single segment, whole, exactly one 128-row block, or
+    one row followed by 127 padding rows."""
+    case = _contig_case(counts, 264, 640, fmt, 3)
+    out = _run_contig(fg, dev, case, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    m_idx, aq, sfa, bq, sfb = case
+    ref, valid = oracle.grouped_contiguous(aq, sfa, bq, sfb, m_idx, fmt)
+    o = out.float().cpu().numpy()
+    rows = m_idx >= 0
+    gemm_close(o[rows], ref[rows], f"contiguous single expert {counts}")
+    assert np.isnan(o[~rows]).all(), "padding rows were written"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("masked", [(200,), (0,), (1,)])
+def test_masked_single_expert(fg, dev, oracle, fmt, masked):
+    """One expert (G = 1) with 200, 0 and 1 valid rows of 256."""
+    case = _masked_case(1, 256, 264, 640, fmt, 4)
+    out = _run_masked(fg, dev, case, masked, fmt)
+    rc, bits = fg.check_status()
+    assert rc == 0, hex(bits)
+    ref, valid = oracle.grouped_masked(*case, np.asarray(masked, np.int32), fmt)
+    o = out.float().cpu().numpy()
+    v = valid.astype(bool)
+    if v.any():
+        gemm_close(o[v], ref[v], f"masked single expert {masked}")
+    assert np.isnan(o[~v]).all(), "rows beyond masked_m were written"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("masked", [(0, 256, 17, 1), (128, 129, 255, 0), (0, 0, 0, 0)])
 def test_masked_small(fg, dev, oracle, fmt, masked):
     case = _masked_case(4, 256, 256, 384, fmt, 2)
