@@ -135,6 +135,15 @@ def test_fp4_gemm_every_tile(fg, dev, oracle, monkeypatch, fmt, tile, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_fp4_gemm_long_k(fg, dev, oracle, fmt):
+    """K = 16384: 64 K blocks of 256 elements, scale groups wrapping the ring many times."""
+    M, N, K = 130, 288, 16384
+    case = _fp4_case(M, N, K, fmt, 61)
+    out = _run(fg, dev, case, fmt, M, N)
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_fp4(*case, fmt), f"fp4 long K fmt{fmt}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_fp4_gemm_full_size(fg, dev, oracle, fmt):
     """M = 4096, N = K = 7168 in the launch configuration the library picks: every
     element against the oracle's dequantize-then-matmul form, plus sampled

@@ -132,6 +132,18 @@ def test_f16_full_size(fg, dev, oracle):
     gemm_close(got[r, c], oracle.gemm_f16_entries(a.float().numpy(), b.float().numpy(), r, c), "f16 (loop)")
 
 
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+def test_f16_long_k(fg, dev, oracle, dt):
+    """K = 16384 + 8: 257 K blocks of 64 elements, the last one 8 wide."""
+    M, N, K = 200, 264, 16392
+    a = inputs.uniform_16bit((M, K), 31, dtype=dt)
+    b = inputs.uniform_16bit((N, K), 32, dtype=dt)
+    out = fg.gemm_f16(a.to(dev), b.to(dev))
+    rc, _ = fg.check_status()
+    assert rc == 0
+    gemm_close(out.float().cpu().numpy(), oracle.gemm_f16(a.float().numpy(), b.float().numpy()), "f16 long K")
+
+
 def test_f16_mixed_output_dtype(fg, dev, oracle):
     a = inputs.uniform_16bit((256, 256), 1)
     b = inputs.uniform_16bit((256, 256), 2)
