@@ -33,6 +33,48 @@ __device__ __forceinline__ int ue8m0_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// x / s rounded to nearest for an FP32 scale s, without the IEEE division
+// routine: Markstein's FMA-based division (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev.
+// 34(1), 1990).  With y = 1/s correctly rounded and a quotient q within one ulp of
+// x / s, the remainder x - q * s is exact in an FMA and q + (x - q * s) * y
+// rounded to nearest is the correctly rounded quotient.  q0 = x * y can be 1.5
+// ulps off, so a first correction makes it faithful and a second rounds it.  The
+// theorem needs every intermediate to stay normal: the remainder is ~2^-23 |x|
+// and |x| >= 2^-10 s wherever the E4M3 code is not zero, so scales from 2^-93 up
+// are safe; smaller ones (groups with max |x| below ~4.5e-26) take the IEEE
+// routine, flagged by y = 0.  The sign is x's, as the quotient's (the correction
+// turns -0 into +0).
+constexpr float kMinFmaDivScale = 0x1p-93f;
+
+__device__ __forceinline__ float scale_reciprocal(float s) {
+  return s >= kMinFmaDivScale ? __frcp_rn(s) : 0.0f;
+}
+
+// Two quotients x0 / s, x1 / s on paired FP32 instructions; y from scale_reciprocal.
+__device__ __forceinline__ void div_by_scale2(float x0, float x1, float s, float y, float& q0, float& q1) {
+  if (y == 0.0f) {
+    q0 = __fdiv_rn(x0, s);
+    q1 = __fdiv_rn(x1, s);
+    return;
+  }
+  float a, b;
+  asm("{\n\t.reg .b64 x, yy, ns, q, e;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 yy, {%4, %4};\n\t"
+      "mov.b64 ns, {%5, %5};\n\t"
+      "mul.rn.f32x2 q, x, yy;\n\t"
+      "fma.rn.f32x2 e, q, ns, x;\n\t"
+      "fma.rn.f32x2 q, e, yy, q;\n\t"
+      "fma.rn.f32x2 e, q, ns, x;\n\t"
+      "fma.rn.f32x2 q, e, yy, q;\n\t"
+      "mov.b64 {%0, %1}, q;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "f"(x0), "f"(x1), "f"(y), "f"(-s));
+  q0 = copysignf(a, x0);
+  q1 = copysignf(b, x1);
+}
+
 // 2^-e as an FP32 value, e in [-127, 127].
 __device__ __forceinline__ float exp2_neg(int e) {
   const int be = 127 - e;

@@ -36,14 +36,20 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
 }
 
 // Quantize 8 values with the group's scale; returns 8 packed E4M3 bytes.  FP32
-// scales divide (x / s, rounded to nearest); power-of-two scales multiply by the
-// exact 2^-e.  The format is a template parameter so each kernel carries only its
-// own arithmetic.
+// scales divide (x / s, rounded to nearest, by quant::div_by_scale2 with inv the
+// scale's reciprocal from quant::scale_reciprocal); power-of-two scales multiply
+// by the exact 2^-e (inv).  The format is a template parameter so each kernel
+// carries only its own arithmetic.
 template <bool UE8M0>
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float inv_pow2) {
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float inv) {
   float q[8];
+  if (UE8M0) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = UE8M0 ? f[i] * inv_pow2 : __fdiv_rn(f[i], s);
+    for (int i = 0; i < 8; ++i) q[i] = f[i] * inv;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) quant::div_by_scale2(f[i], f[i + 1], s, inv, q[i], q[i + 1]);
+  }
   uint2 r;
   r.x = static_cast<uint32_t>(ptx::cvt_e4m3x2(q[0], q[1])) |
         (static_cast<uint32_t>(ptx::cvt_e4m3x2(q[2], q[3])) << 16);
@@ -102,8 +108,9 @@ __device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item
   if (UE8M0) {
     e = ue8m0_exponent(amax);
     inv = exp2_neg(e);
-  } else if (amax != 0.0f) {
-    s = __fdiv_rn(amax, kE4M3Max);
+  } else {
+    if (amax != 0.0f) s = __fdiv_rn(amax, kE4M3Max);
+    inv = quant::scale_reciprocal(s);
   }
   if (t.active) {
     const uint2 lo = quant8<UE8M0>(f0, s, inv), hi = quant8<UE8M0>(f1, s, inv);
@@ -220,8 +227,9 @@ __global__ void __launch_bounds__(256, 3) quantize_128x128_kernel(const __nv_bfl
   if (UE8M0) {
     e = ue8m0_exponent(amax);
     inv = exp2_neg(e);
-  } else if (amax != 0.0f) {
-    s = __fdiv_rn(amax, kE4M3Max);
+  } else {
+    if (amax != 0.0f) s = __fdiv_rn(amax, kE4M3Max);
+    inv = quant::scale_reciprocal(s);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {

@@ -64,3 +64,41 @@ def test_quantize_empty_is_noop(fg, dev):
     x = torch.empty((0, 256), dtype=torch.bfloat16, device=dev)
     xq, sfa = fg.quantize_1x128(x, 0)
     assert xq.shape == (0, 256)
+
+
+def _every_value_under_many_scales():
+    """1x128 groups led by amax, then every bf16 value of magnitude <= amax (both
+    signs), for amax = every bf16 significand at exponents from 2^-100 to 2^100.
+    The FP32 scales amax / 448 then run through all significand patterns of the
+    scale's top bits, and the codes cover every E4M3 rounding decision each scale
+    can see, ties included; 2^-100 and 2^-60 groups sit on either side of the
+    scale below which the kernels divide with the IEEE routine."""
+    bits = np.arange(0x8000, dtype=np.uint32)
+    pos = (bits << 16).view(np.float32)
+    pos = pos[np.isfinite(pos)]
+    groups = []
+    for e in (-100, -60, -20, -8, -1, 0, 1, 3, 7, 15, 40, 100):
+        for m in range(128):
+            amax = np.float32(np.ldexp(1.0 + m / 128.0, e))
+            vals = pos[pos <= amax]
+            vals = np.concatenate([vals, -vals])
+            vals = np.concatenate([vals, np.zeros((-len(vals)) % 127, np.float32)])
+            body = vals.reshape(-1, 127)
+            groups.append(np.concatenate([np.full((len(body), 1), amax, np.float32), body], axis=1))
+    g = np.concatenate(groups).reshape(-1)
+    g = np.concatenate([g, np.zeros((-len(g)) % 4096, np.float32)])
+    return torch.from_numpy(g.reshape(-1, 4096)).to(torch.bfloat16)
+
+
+def test_quantize_1x128_f32_scales_every_value(fg, dev, oracle):
+    """FP32 scales: the kernels divide by the scale without the IEEE division
+    routine (Markstein's FMA division); every code must still equal the oracle's,
+    which divides in IEEE arithmetic.  About 60 M values under 1536 scales."""
+    x = _every_value_under_many_scales()
+    xq, sfa = fg.quantize_1x128(x.to(dev), 0)
+    oq, osf = oracle.quantize_1x128(x.float().numpy(), 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(sfa.cpu().numpy().view(np.uint8), osf.view(np.uint8)), "scales differ"
+    got = xq.cpu().numpy()
+    bad = np.nonzero(got != oq)
+    assert bad[0].size == 0, f"{bad[0].size} codes differ, first at {bad[0][0]}, {bad[1][0]}"
