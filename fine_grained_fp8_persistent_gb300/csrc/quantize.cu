@@ -132,7 +132,7 @@ __device__ __forceinline__ void quant_item_1x128(const uint4 (&w)[2], const Item
 }
 
 template <bool UE8M0>
-__global__ void __launch_bounds__(256) quantize_1x128_kernel(const __nv_bfloat16* __restrict__ X,
+__global__ void __launch_bounds__(256, 3) quantize_1x128_kernel(const __nv_bfloat16* __restrict__ X,
                                                              uint8_t* __restrict__ Xq,
                                                              void* __restrict__ SF, int M, int K,
                                                              int per_warp) {
