@@ -336,7 +336,8 @@ struct PCfg {
   static constexpr int MMA_K_BYTES = 32;
   static constexpr int MMAS_PER_STAGE = 128 / MMA_K_BYTES;
   // Rows of A per K block.  A thin tile (AROWS = 64, for a dense GEMM with at most
-  // 64 rows) loads 64-row A boxes.  With FP32 scales it also stages 64 rows and
+  // 64 rows) stages 64 A rows, loaded by a box of M rounded up to 8 rows
+  // (args.a_box_rows; the stage rows past it are never stored).  With FP32 scales it
   // issues M = 64 MMAs ("Blackwell Tensor Core: tcgen05.mma": the cta_group::1
   // M = 64 accumulator, Layout F, puts row m in TMEM lane 32 (m / 16) + m % 16, so
   // each lane quarter holds 16 rows in its first 16 lanes), which leaves room for
