@@ -144,7 +144,15 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
                                      : "f8f32",
                 SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN,
                 C::kWS ? "ws" : "");
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, la);
+  // the dense output map of the TMA-store epilogue: 32 x 32 boxes of 16-bit values
+  CUtensorMap tm_d;
+  std::memset(&tm_d, 0, sizeof(tm_d));
+  if constexpr (C::kTmaStore) {
+    if (!encode_tmap_2d(&tm_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.D, static_cast<uint64_t>(a.N),
+                        static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.N) * 2u, 32, 32, false))
+      return 4;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, tm_d, la);
   if (e != cudaSuccess) return set_error(4, "gemm launch: %s", cudaGetErrorString(e));
   return 0;
 }

@@ -459,7 +459,18 @@ struct PCfg {
                                                                : 0;
   // staging response (16 bytes), then CLC_Q published tile ids (int32, -1 = end)
   static constexpr int OFF_CLC = (OFF_PREFIX + PREFIX_BYTES + 15) / 16 * 16;
-  static constexpr int SMEM_BYTES = OFF_CLC + 16 + 4 * CLC_Q + 1024;
+  // Dense output without masked rows: the epilogue stages each warp's 32 x 32
+  // chunk of D in shared memory (two buffers per warp) and writes it with a TMA
+  // tensor store, one coalesced bulk transfer instead of 32 rows of 16-byte
+  // stores per instruction.  Grouped layouts keep per-row stores (rows that must
+  // not be written).
+  static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 2;
+  static constexpr int OFF_EPI = (OFF_CLC + 16 + 4 * CLC_Q + 127) / 128 * 128;
+  static constexpr bool kTmaStore = SCHED == Sched::Dense && !QOUT_ && !kF32S && NACC_ == 2 && !kWS &&
+                                    BN % 32 == 0 && QROWS == 32 &&
+                                    OFF_EPI + 2 * EPI_WARPS * EPI_CHUNK_BYTES + 1024 <= 232448;
+  static constexpr int EPI_BYTES = kTmaStore ? 2 * EPI_WARPS * EPI_CHUNK_BYTES : 0;
+  static constexpr int SMEM_BYTES = OFF_EPI + EPI_BYTES + 1024;
 
   static constexpr int ACC_COLS = NACC * PBN;
   static constexpr int SF_COL0 = ACC_COLS;
@@ -535,6 +546,10 @@ __device__ __forceinline__ uint32_t pack_2x16(float a, float b, bool bf16) {
   }
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // 32 consecutive FP32 values of one output row -> 16-bit, columns col0..col0+31
@@ -662,7 +677,8 @@ template <Kind KIND, Sched SCHED, int NCTA, int BN, int STAGES, int NACC, int AR
 __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>::THREADS, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
-                    const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tm_sfb,
+                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
   using C = PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROWS, QOUT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -703,6 +719,7 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       ptx::prefetch_tmap(&tm_sfa);
       ptx::prefetch_tmap(&tm_sfb);
     }
+    if constexpr (C::kTmaStore) ptx::prefetch_tmap(&tm_d);
   }
   if (threadIdx.x == 0) {
     for (int u = 0; u < C::UNITS; ++u) {
@@ -1282,6 +1299,8 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
     const bool bf16 = args.out_bf16 != 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t epi_chunks = 0;   // chunks staged so far (TMA-store epilogue)
+    (void)epi_chunks;
     bool ok = true;
     for (Seq sq = seq_begin(); sq.t != kSeqEnd; seq_step_epi(sq)) {
       Tile tl;
@@ -1341,6 +1360,44 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       // the accumulator is released after its last load
       constexpr int NCH = BN / 32;
       constexpr bool TAIL = (BN % 32) != 0;
+      if constexpr (C::kTmaStore) {
+        // each chunk, rounded to 16 bits, goes to one of this warp's two staging
+        // buffers (row `lane` = 64 bytes) and lane 0 stores it by TMA; the buffer
+        // is rewritten only after the store issued two chunks earlier has read it
+        const uint32_t stage0 = sbase + C::OFF_EPI + (warp - C::EPI_WARP0) * 2u * C::EPI_CHUNK_BYTES;
+        const int y = tl.a_row0 + static_cast<int>(q) * 32;     // first row of this warp's 32
+#pragma unroll 1
+        for (int c = 0; c < NCH; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + 32u * c, v);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(v);
+          if (c == NCH - 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lbar(C::BAR_ACC_EMPTY + acc));
+          }
+          const uint32_t buf = stage0 + (epi_chunks & 1u) * C::EPI_CHUNK_BYTES;
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float* f = reinterpret_cast<const float*>(v) + 8 * j;
+            st_shared_v4(buf + lane * 64u + 16u * j, pack_2x16(f[0], f[1], bf16), pack_2x16(f[2], f[3], bf16),
+                         pack_2x16(f[4], f[5], bf16), pack_2x16(f[6], f[7], bf16));
+          }
+          ptx::fence_proxy_async_smem();   // the generic writes, before the async-proxy read
+          __syncwarp();
+          const int x = tl.n_blk * BN + 32 * c;
+          if (lane == 0 && y < M && x < N) {
+            ptx::tma_store_2d(&tm_d, buf, x, y);
+            ptx::bulk_commit_group();
+          }
+          ++epi_chunks;
+        }
+        if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < NCH; ++c) {
         uint32_t v[32];
@@ -1367,6 +1424,11 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
           store_row16(args.D, row_off, tl.n_blk * BN + 32 * NCH, N, reinterpret_cast<const float*>(v), bf16);
       }
       if (++acc == C::NACC) { acc = 0; acc_phase ^= 1u; }
+    }
+    if constexpr (C::kTmaStore) {
+      // every store this warp issued has completed before the CTA may exit
+      if (lane == 0) ptx::bulk_wait_group<0>();
+      __syncwarp();
     }
     aborted = !ok;
   } else if constexpr (!C::kF32S) {
