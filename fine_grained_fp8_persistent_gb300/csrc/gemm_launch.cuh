@@ -144,12 +144,14 @@ int launch_persistent(const GemmArgs& a, const TensorMaps& tm, long long tiles, 
                                      : "f8f32",
                 SCHED == Sched::Dense ? "dense" : SCHED == Sched::Contiguous ? "contiguous" : "masked", CL, BN,
                 C::kWS ? "ws" : "");
-  // the dense output map of the TMA-store epilogue: 32 x 32 boxes of 16-bit values
+  // the output map of the TMA-store epilogue: 32 x 32 boxes of 16-bit values
   CUtensorMap tm_d;
   std::memset(&tm_d, 0, sizeof(tm_d));
   if constexpr (C::kTmaStore) {
-    if (!encode_tmap_2d(&tm_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.D, static_cast<uint64_t>(a.N),
-                        static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.N) * 2u, 32, 32, false))
+    // rows of D: M (dense, contiguous) or G x Mmax (masked, experts stacked)
+    const uint64_t d_rows = static_cast<uint64_t>(a.M) * (SCHED == Sched::Masked ? static_cast<uint64_t>(a.G) : 1u);
+    if (!encode_tmap_2d(&tm_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.D, static_cast<uint64_t>(a.N), d_rows,
+                        static_cast<uint64_t>(a.N) * 2u, 32, 32, false))
       return 4;
   }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, tm.a, tm.b, tm.sfa, tm.sfb, tm_d, la);

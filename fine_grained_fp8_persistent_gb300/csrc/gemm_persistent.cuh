@@ -459,14 +459,15 @@ struct PCfg {
                                                                : 0;
   // staging response (16 bytes), then CLC_Q published tile ids (int32, -1 = end)
   static constexpr int OFF_CLC = (OFF_PREFIX + PREFIX_BYTES + 15) / 16 * 16;
-  // Dense output without masked rows: the epilogue stages each warp's 32 x 32
-  // chunk of D in shared memory (two buffers per warp) and writes it with a TMA
-  // tensor store, one coalesced bulk transfer instead of 32 rows of 16-byte
-  // stores per instruction.  Grouped layouts keep per-row stores (rows that must
-  // not be written).
+  // The epilogue stages each warp's 32 x 32 chunk of D in shared memory (two
+  // buffers per warp) and writes it with a TMA tensor store, one coalesced bulk
+  // transfer instead of 32 rows of 16-byte stores per instruction.  In grouped
+  // layouts a warp does so only when all its 32 rows are to be written (rows
+  // past masked_m and padding rows must stay untouched); otherwise it stores
+  // its valid rows one by one.
   static constexpr int EPI_CHUNK_BYTES = 32 * 32 * 2;
   static constexpr int OFF_EPI = (OFF_CLC + 16 + 4 * CLC_Q + 127) / 128 * 128;
-  static constexpr bool kTmaStore = SCHED == Sched::Dense && !QOUT_ && !kF32S && NACC_ == 2 && !kWS &&
+  static constexpr bool kTmaStore = !QOUT_ && !kF32S && NACC_ == 2 && !kWS &&
                                     BN % 32 == 0 && QROWS == 32 &&
                                     OFF_EPI + 2 * EPI_WARPS * EPI_CHUNK_BYTES + 1024 <= 232448;
   static constexpr int EPI_BYTES = kTmaStore ? 2 * EPI_WARPS * EPI_CHUNK_BYTES : 0;
@@ -1360,7 +1361,10 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
       // the accumulator is released after its last load
       constexpr int NCH = BN / 32;
       constexpr bool TAIL = (BN % 32) != 0;
-      if constexpr (C::kTmaStore) {
+      // dense: the tensor map clips rows past M; grouped: every row of the warp valid
+      bool tma_rows = true;
+      if constexpr (C::kTmaStore && SCHED != Sched::Dense) tma_rows = __all_sync(0xffffffffu, row_ok);
+      if (C::kTmaStore && tma_rows) {
         // each chunk, rounded to 16 bits, goes to one of this warp's two staging
         // buffers (row `lane` = 64 bytes) and lane 0 stores it by TMA; the buffer
         // is rewritten only after the store issued two chunks earlier has read it
@@ -1389,7 +1393,9 @@ __global__ void __launch_bounds__(PCfg<KIND, SCHED, NCTA, BN, STAGES, NACC, AROW
           ptx::fence_proxy_async_smem();   // the generic writes, before the async-proxy read
           __syncwarp();
           const int x = tl.n_blk * BN + 32 * c;
-          if (lane == 0 && y < M && x < N) {
+          // rows of D's 2-D view: M, or G x Mmax with the experts stacked (masked)
+          const int d_rows = SCHED == Sched::Masked ? G * M : M;
+          if (lane == 0 && y < d_rows && x < N) {
             ptx::tma_store_2d(&tm_d, buf, x, y);
             ptx::bulk_commit_group();
           }
